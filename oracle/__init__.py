@@ -1,0 +1,10 @@
+"""CPU oracle (test infrastructure only; never imported by the product path)."""
+from .attention import (  # noqa: F401
+    backward,
+    delta,
+    forward,
+    sequences,
+    sparse_backward,
+    sparse_forward,
+    visible,
+)
