@@ -1,0 +1,24 @@
+"""GB300-native fused softmax-attention backward.
+
+The compute lives in the CUDA library ``_build/libattn_bwd.so`` (C ABI,
+``include/attn_bwd.h``); this package only marshals torch tensors into that
+ABI.  There is no CPU path: every call fails loudly when the library or a
+CUDA device is missing.
+"""
+from ._binding import (  # noqa: F401
+    AttnBwdError,
+    LIB_PATH,
+    attn_bwd,
+    attn_bwd_gqa,
+    attn_bwd_sparse,
+    backward,
+    check_error,
+    dq_land,
+    library,
+    preprocess,
+    query_block_range,
+    selftest_timeout,
+    sparse_backward,
+    sparse_land,
+    workspace_size,
+)

@@ -1,0 +1,264 @@
+"""ctypes binding of the C ABI in ``include/attn_bwd.h``.
+
+Argument marshalling only: torch tensors are turned into device pointers and
+element strides, the current torch CUDA stream into a cudaStream_t, and
+non-zero status codes into ``AttnBwdError``.  Every arithmetic step runs in
+the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libattn_bwd.so")
+
+c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+DT_F16, DT_BF16 = 0, 1
+
+
+class AttnBwdError(RuntimeError):
+    pass
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", c_i64), ("s", c_i64), ("h", c_i64)]
+
+
+class Mask(ctypes.Structure):
+    _fields_ = [("causal", c_i32), ("window_left", c_i32), ("cu_seqlens", c_vp), ("num_seqs", c_i32)]
+
+
+_SIGS = {
+    "attn_bwd_workspace_size": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
+    "attn_bwd_preprocess": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                    c_i64, c_i32, c_vp, c_sz, c_vp]),
+    "attn_bwd_gqa": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64,
+                             c_i64, c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, c_sz,
+                             c_vp]),
+    "attn_bwd": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64,
+                         c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd_dq_land": (c_i32, [c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, c_sz, c_vp]),
+    "attn_bwd_sparse": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64,
+                                c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, c_sz, c_vp]),
+    "attn_bwd_sparse_land": (c_i32, [c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32,
+                                     c_vp, c_sz, c_vp]),
+    "attn_bwd_check_error": (c_i32, [c_vp, c_vp, ctypes.POINTER(c_i32)]),
+    "attn_bwd_status_string": (ctypes.c_char_p, [c_i32]),
+    "attn_bwd_query_block_range": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
+                                          ctypes.POINTER(c_i32)]),
+    "attn_bwd_selftest_timeout": (c_i32, [c_vp, c_sz, c_i32, c_vp]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise AttnBwdError(f"CUDA library missing at {LIB_PATH}: build it with attention_backward_gb300.build")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _status(code: int, what: str) -> None:
+    if code != 0:
+        msg = library().attn_bwd_status_string(code).decode()
+        raise AttnBwdError(f"{what}: {msg} (status {code})")
+
+
+def _dev(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise AttnBwdError("attention backward tensors must be CUDA tensors")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return DT_F16
+    if t.dtype == torch.bfloat16:
+        return DT_BF16
+    raise AttnBwdError(f"unsupported dtype {t.dtype}: fp16 or bf16")
+
+
+def _bshd(t: torch.Tensor) -> Strides:
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise AttnBwdError("expected a BSHD tensor with a contiguous head dimension")
+    return Strides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _lse_strides(lse: torch.Tensor) -> Strides:
+    if lse.dim() != 3 or lse.dtype != torch.float32:
+        raise AttnBwdError("lse must be float32 [B, H, S]")
+    return Strides(lse.stride(0), lse.stride(2), lse.stride(1))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _mask(causal: bool, window: int, cu_seqlens: Optional[torch.Tensor]) -> Mask:
+    m = Mask(1 if causal else 0, int(window), None, 0)
+    if cu_seqlens is not None:
+        _dev(cu_seqlens)
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+            raise AttnBwdError("cu_seqlens must be a contiguous int32 vector")
+        m.cu_seqlens = cu_seqlens.data_ptr()
+        m.num_seqs = cu_seqlens.numel() - 1
+    return m
+
+
+def workspace_size(B: int, S: int, H: int, Dq: int, dkv_elems: int = 0) -> int:
+    return int(library().attn_bwd_workspace_size(B, S, H, Dq, dkv_elems))
+
+
+def new_workspace(B: int, S: int, H: int, Dq: int, dkv_elems: int = 0, device=None) -> torch.Tensor:
+    n = workspace_size(B, S, H, Dq, dkv_elems)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def preprocess(o, do, lse, workspace, Dq: Optional[int] = None, dkv_elems: int = 0, stream=None) -> None:
+    """Launch 1: delta, LSE*log2(e), zeroed accumulators (see attn_bwd_preprocess)."""
+    _dev(o, do, lse, workspace)
+    B, S, H, Dv = o.shape
+    Dq = Dv if Dq is None else Dq
+    _status(library().attn_bwd_preprocess(o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(),
+                                          _lse_strides(lse), B, S, H, Dv, Dq, dkv_elems, _dt(o),
+                                          workspace.data_ptr(), workspace.numel(), _stream(stream)),
+            "attn_bwd_preprocess")
+
+
+def attn_bwd_gqa(q, k, v, do, dk, dv, workspace, sm_scale: float, causal: bool = False, window: int = -1,
+                 cu_seqlens=None, stream=None) -> None:
+    """Launch 2: dK, dV written, dQ accumulated in the workspace (see attn_bwd_gqa)."""
+    _dev(q, k, v, do, dk, dv, workspace)
+    B, S, HQ, D = q.shape
+    HKV = k.shape[2]
+    m = _mask(causal, window, cu_seqlens)
+    _status(library().attn_bwd_gqa(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
+                                   do.data_ptr(), _bshd(do), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
+                                   ctypes.byref(m), dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv),
+                                   workspace.data_ptr(), workspace.numel(), _stream(stream)), "attn_bwd_gqa")
+
+
+def attn_bwd(q, k, v, do, dk, dv, workspace, sm_scale: float, causal: bool = False, window: int = -1,
+             cu_seqlens=None, stream=None) -> None:
+    """Launch 2 for multi-head attention (HQ == HKV)."""
+    _dev(q, k, v, do, dk, dv, workspace)
+    B, S, H, D = q.shape
+    m = _mask(causal, window, cu_seqlens)
+    _status(library().attn_bwd(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
+                               do.data_ptr(), _bshd(do), B, S, H, D, _dt(q), float(sm_scale), ctypes.byref(m),
+                               dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv), workspace.data_ptr(),
+                               workspace.numel(), _stream(stream)), "attn_bwd")
+
+
+def dq_land(dq, workspace, sm_scale: float, stream=None) -> None:
+    """Launch 3: dQ = cast(sm_scale * dQacc)."""
+    _dev(dq, workspace)
+    B, S, H, D = dq.shape
+    _status(library().attn_bwd_dq_land(dq.data_ptr(), _bshd(dq), B, S, H, D, _dt(dq), float(sm_scale),
+                                       workspace.data_ptr(), workspace.numel(), _stream(stream)),
+            "attn_bwd_dq_land")
+
+
+def attn_bwd_sparse(q, kv, do, idx, workspace, sm_scale: float, dv_dim: int, stream=None) -> None:
+    """Launch 2 of the top-k sparse path (see attn_bwd_sparse)."""
+    _dev(q, kv, do, idx, workspace)
+    B, S, H, DQK = q.shape
+    SKV, HKV = kv.shape[1], kv.shape[2]
+    if idx.dtype != torch.int32 or idx.dim() != 4 or idx.stride(3) != 1:
+        raise AttnBwdError("idx must be int32 [B, S, HKV, topk] with unit slot stride")
+    topk = idx.shape[3]
+    _status(library().attn_bwd_sparse(q.data_ptr(), _bshd(q), kv.data_ptr(), _bshd(kv), do.data_ptr(), _bshd(do),
+                                      idx.data_ptr(), Strides(idx.stride(0), idx.stride(1), idx.stride(2)), B, S,
+                                      SKV, H, HKV, DQK, dv_dim, topk, _dt(q), float(sm_scale),
+                                      workspace.data_ptr(), workspace.numel(), _stream(stream)), "attn_bwd_sparse")
+
+
+def sparse_land(dq, dkv, workspace, stream=None) -> None:
+    """Launch 3 of the sparse path: dQ and dKV cast from their accumulators."""
+    _dev(dq, dkv, workspace)
+    B, S, H, DQK = dq.shape
+    SKV, HKV = dkv.shape[1], dkv.shape[2]
+    _status(library().attn_bwd_sparse_land(dq.data_ptr(), _bshd(dq), dkv.data_ptr(), _bshd(dkv), B, S, SKV, H, HKV,
+                                           DQK, _dt(dq), workspace.data_ptr(), workspace.numel(), _stream(stream)),
+            "attn_bwd_sparse_land")
+
+
+def check_error(workspace, stream=None) -> int:
+    """Synchronises the stream; raises if a kernel recorded a device error."""
+    code = c_i32(0)
+    st = library().attn_bwd_check_error(workspace.data_ptr(), _stream(stream), ctypes.byref(code))
+    if st != 0:
+        msg = library().attn_bwd_status_string(st).decode()
+        raise AttnBwdError(f"device error: {msg} (site 0x{code.value:x})")
+    return 0
+
+
+def selftest_timeout(workspace, timeout_us: int = 20000, stream=None) -> tuple:
+    """Runs the bounded-wait self-test; returns (status, status string)."""
+    st = library().attn_bwd_selftest_timeout(workspace.data_ptr(), workspace.numel(), int(timeout_us),
+                                             _stream(stream))
+    return st, library().attn_bwd_status_string(st).decode()
+
+
+def query_block_range(k0: int, block_k: int, length: int, causal: bool, window: int, block_q: int) -> tuple:
+    lo, hi = c_i32(0), c_i32(0)
+    library().attn_bwd_query_block_range(k0, block_k, length, int(causal), int(window), block_q, ctypes.byref(lo),
+                                         ctypes.byref(hi))
+    return lo.value, hi.value
+
+
+def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1,
+             cu_seqlens=None, workspace=None, stream=None):
+    """dQ, dK, dV of softmax attention: the three launches on one stream.
+
+    q, o, do: [B,S,HQ,D]; k, v: [B,S,HKV,D] (fp16/bf16, CUDA); lse: f32 [B,HQ,S]
+    (natural log).  Outputs are new tensors in the input dtype.
+    """
+    _dev(q, k, v, o, do, lse)
+    B, S, HQ, D = q.shape
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if workspace is None:
+        workspace = new_workspace(B, S, HQ, D, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    preprocess(o, do, lse, workspace, Dq=D, stream=stream)
+    attn_bwd_gqa(q, k, v, do, dk, dv, workspace, sm_scale, causal, window, cu_seqlens, stream)
+    dq_land(dq, workspace, sm_scale, stream)
+    return dq, dk, dv
+
+
+def sparse_backward(q, kv, o, do, lse, idx, sm_scale: Optional[float] = None, dv_dim: Optional[int] = None,
+                    workspace=None, stream=None):
+    """dQ and dKV of top-k sparse attention over shared latent rows."""
+    _dev(q, kv, o, do, lse, idx)
+    B, S, H, DQK = q.shape
+    SKV, HKV = kv.shape[1], kv.shape[2]
+    dv_dim = do.shape[3] if dv_dim is None else dv_dim
+    if sm_scale is None:
+        sm_scale = DQK ** -0.5
+    dkv_elems = B * SKV * HKV * DQK
+    if workspace is None:
+        workspace = new_workspace(B, S, H, DQK, dkv_elems, device=q.device)
+    dq = torch.empty_like(q)
+    dkv = torch.empty_like(kv)
+    preprocess(o, do, lse, workspace, Dq=DQK, dkv_elems=dkv_elems, stream=stream)
+    attn_bwd_sparse(q, kv, do, idx, workspace, sm_scale, dv_dim, stream)
+    sparse_land(dq, dkv, workspace, stream)
+    return dq, dkv

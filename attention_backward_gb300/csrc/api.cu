@@ -1,0 +1,237 @@
+// Host entry points of the C ABI declared in include/attn_bwd.h: argument
+// validation, workspace layout, TMA descriptors and launches.  Nothing here
+// allocates device memory or keeps state between calls other than the
+// driver entry point of cuTensorMapEncodeTiled, looked up once.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_bwd.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using namespace ab;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// BSHD strides (elements) of a 16-bit tensor: positive, 16-byte multiples,
+// within the TMA stride limit.
+bool strides_ok(const attn_strides_t& s) {
+  auto one = [](int64_t x) { return x > 0 && ((x * 2) % 16) == 0 && x * 2 < (int64_t(1) << 40); };
+  return one(s.b) && one(s.s) && one(s.h);
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+attn_status_t launch_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
+
+// 4-D tiled map over a BSHD 16-bit tensor: dims (D, H, S, B), box (64, 1,
+// rows, 1), 128-byte swizzle (the layout the tcgen05 descriptors expect).
+bool make_map(CUtensorMap* m, const void* base, attn_dtype_t dt, int64_t B, int64_t S, int64_t H, int64_t D,
+              const attn_strides_t& st, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h * 2), static_cast<cuuint64_t>(st.s * 2),
+                           static_cast<cuuint64_t>(st.b * 2)};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty = dt == ATTN_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, ty, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t wait_limit_ns() { return ab::kWaitTimeoutNs; }
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(int64_t B, int64_t S, int64_t H, int64_t Dq, int64_t dkv_elems) {
+  if (B < 0 || S < 0 || H < 0 || Dq < 0 || dkv_elems < 0) return 0;
+  return static_cast<size_t>(ws_layout(B, S, H, Dq, dkv_elems).total);
+}
+
+const char* attn_bwd_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_LAUNCH: return "kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case ATTN_ERR_DEVICE: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_t len, int32_t causal, int32_t window_left,
+                                int32_t block_q, int32_t* lo, int32_t* hi) {
+  int l = 0, h = 0;
+  if (block_k > 0 && block_q > 0) query_block_range(k0, block_k, len, causal, window_left, block_q, &l, &h);
+  if (lo) *lo = l;
+  if (hi) *hi = h;
+}
+
+attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                                  const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t H,
+                                  int64_t Dv, int64_t Dq, int64_t dkv_elems, attn_dtype_t dtype, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!o || !dO || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || Dv < 8 || Dv % 8 || Dv > 1024 || Dq < 8 || Dq % 8 || dkv_elems < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace) || !strides_ok(so) || !strides_ok(sdo))
+    return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, S, H, Dq, dkv_elems);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PreprocessParams p{};
+  p.o = static_cast<const uint8_t*>(o);
+  p.so_b = so.b, p.so_s = so.s, p.so_h = so.h;
+  p.dO = static_cast<const uint8_t*>(dO);
+  p.sdo_b = sdo.b, p.sdo_s = sdo.s, p.sdo_h = sdo.h;
+  p.lse = lse;
+  p.sl_b = slse.b, p.sl_s = slse.s, p.sl_h = slse.h;
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.Dv = static_cast<int>(Dv);
+  p.lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<float*>(ws + L.delta_off);
+  p.zero = reinterpret_cast<float4*>(ws + L.dq_off);
+  p.zero_n4 = (L.total - L.dq_off) / 16;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  return launch_status(launch_preprocess(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                           attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S,
+                           int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
+                           const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !dO || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || HQ < 1 || HKV < 1 || HQ % HKV != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (S >= (int64_t(1) << 31) || B * HQ * S >= (int64_t(1) << 31) || B > 65535 || HQ > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, k, v, dO, static_cast<const void*>(dk), static_cast<const void*>(dv),
+                          static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  for (const attn_strides_t* s : {&sq, &sk, &sv, &sdo, &sdk, &sdv})
+    if (!strides_ok(*s)) return ATTN_ERR_INVALID_ARG;
+  int causal = 0, window = -1, num_seqs = 0;
+  const int32_t* cu = nullptr;
+  if (mask) {
+    causal = mask->causal ? 1 : 0;
+    window = mask->window_left;
+    cu = mask->cu_seqlens;
+    num_seqs = mask->num_seqs;
+    if (window == 0 || window < -1) return ATTN_ERR_INVALID_ARG;
+    if (cu && (B != 1 || num_seqs < 1 || num_seqs > (1 << 20))) return ATTN_ERR_INVALID_ARG;
+  }
+  const WsLayout L = ws_layout(B, S, HQ, D, 0);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  const int BN = dense_bn(static_cast<int>(D));
+  DenseMaps m;
+  if (!make_map(&m.q, q, dtype, B, S, HQ, D, sq, BN) || !make_map(&m.dO, dO, dtype, B, S, HQ, D, sdo, BN) ||
+      !make_map(&m.k, k, dtype, B, S, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, S, HKV, D, sv, kDenseBM))
+    return ATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DenseParams p{};
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV);
+  p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D);
+  p.causal = causal, p.window = window, p.cu_seqlens = cu, p.num_seqs = num_seqs;
+  p.sm_scale = sm_scale;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
+  p.dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
+  p.err = &reinterpret_cast<WsHeader*>(ws)->err;
+  p.dk = static_cast<uint8_t*>(dk), p.sdk_b = sdk.b, p.sdk_s = sdk.s, p.sdk_h = sdk.h;
+  p.dv = static_cast<uint8_t*>(dv), p.sdv_b = sdv.b, p.sdv_s = sdv.s, p.sdv_h = sdv.h;
+  p.timeout_ns = wait_limit_ns();
+  // key tiles per (batch, KV head): a packed batch may add one partial tile per sequence
+  const int64_t tiles = (S + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0);
+  const int64_t grid = tiles * B * HKV;
+  if (grid >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  return launch_status(launch_dense(p, m, dtype == ATTN_DT_BF16, static_cast<int>(grid),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                       attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S, int64_t H,
+                       int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dk,
+                       attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return attn_bwd_gqa(q, sq, k, sk, v, sv, dO, sdo, B, S, H, H, D, dtype, sm_scale, mask, dk, sdk, dv, sdv,
+                      workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
+                               attn_dtype_t dtype, float sm_scale, const void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (!dq || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || D < 8 || D % 8) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(dq) || !aligned16(workspace) || !strides_ok(sdq)) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, S, H, D, 0);
+  if (workspace_bytes < static_cast<size_t>(L.dkv_off)) return ATTN_ERR_WORKSPACE;
+  LandParams p{};
+  p.acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + L.dq_off);
+  p.rows = B * S * H;
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.D = static_cast<int>(D);
+  p.out = static_cast<uint8_t*>(dq);
+  p.s_b = sdq.b, p.s_s = sdq.s, p.s_h = sdq.h;
+  p.scale = sm_scale;
+  return launch_status(launch_land(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd_check_error(const void* workspace, void* stream, int32_t* device_code) {
+  if (device_code) *device_code = 0;
+  if (!workspace) return ATTN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_DEVICE;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_DEVICE;
+  if (device_code) *device_code = h.err;
+  return h.err == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+attn_status_t attn_bwd_selftest_timeout(void* workspace, size_t workspace_bytes, int32_t timeout_us, void* stream) {
+  if (!workspace || workspace_bytes < static_cast<size_t>(kHeaderBytes) || timeout_us < 1 || timeout_us > 10000000)
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kHeaderBytes, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (launch_selftest_timeout(&static_cast<WsHeader*>(workspace)->err, static_cast<uint64_t>(timeout_us) * 1000ull,
+                              st) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  return attn_bwd_check_error(workspace, stream, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Parameter blocks and launchers of the kernels (internal to the library).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace ab {
+
+struct PreprocessParams {
+  const uint8_t* o;
+  int64_t so_b, so_s, so_h;  // element strides
+  const uint8_t* dO;
+  int64_t sdo_b, sdo_s, sdo_h;
+  const float* lse;
+  int64_t sl_b, sl_s, sl_h;
+  int B, S, H, Dv;
+  float* lse2;   // [B,H,S]
+  float* delta;  // [B,H,S]
+  float4* zero;  // accumulators to clear
+  int64_t zero_n4;
+  WsHeader* hdr;
+};
+
+struct LandParams {
+  const float* acc;  // [rows = B*S*H][D] f32
+  int64_t rows;
+  int B, S, H, D;
+  uint8_t* out;  // 16-bit BSHD
+  int64_t s_b, s_s, s_h;
+  float scale;
+};
+
+struct DenseParams {
+  int B, S, HQ, HKV, G, D;
+  int causal, window;
+  const int* cu_seqlens;
+  int num_seqs;
+  float scale_log2;  // sm_scale * log2(e)
+  float sm_scale;
+  const float* lse2;   // [B,HQ,S]
+  const float* delta;  // [B,HQ,S]
+  float* dq_acc;       // [B,S,HQ,D]
+  int* err;
+  uint8_t* dk;
+  int64_t sdk_b, sdk_s, sdk_h;
+  uint8_t* dv;
+  int64_t sdv_b, sdv_s, sdv_h;
+  uint64_t timeout_ns;
+};
+
+struct DenseMaps {
+  CUtensorMap q, k, v, dO;
+};
+
+cudaError_t launch_preprocess(const PreprocessParams& p, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_land(const LandParams& p, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);
+cudaError_t launch_selftest_timeout(int* err, uint64_t timeout_ns, cudaStream_t st);
+
+// Block sizes of the dense kernel (keys per tile, queries per step).
+constexpr int kDenseBM = 128;
+__host__ __device__ constexpr int dense_bn(int D) { return D == 128 ? 64 : 128; }
+
+}  // namespace ab

@@ -1,0 +1,192 @@
+/*
+ * attn_bwd.h -- C ABI of the GB300 (sm_103a) fused softmax-attention backward.
+ *
+ * Given Q, K, V, O, dO and the per-row natural-log log-sum-exp of a softmax
+ * attention forward, the library computes dQ, dK and dV without materialising
+ * any S x S matrix.  The operation is the unsplit backward of the TileOPs pull
+ * request "Serve MHA backward on a warp-specialized SM90 kernel and time FA3's
+ * backward alone" (section "TileFoundry Description", program "Reference"):
+ *
+ *   delta_i = sum_d O_id dO_id
+ *   P_ij    = exp(scale * q_i.k_j - LSE_i)   where key j is visible to query i, else 0
+ *   dV_j    = sum_i P_ij dO_i
+ *   dP_ij   = dO_i . v_j
+ *   dS_ij   = P_ij (dP_ij - delta_i) scale
+ *   dQ_i    = sum_j dS_ij k_j                 dK_j = sum_i dS_ij q_i
+ *
+ * split, as on that page's "Tiled" program and its three-launch summary, into
+ * a preprocess (delta), a main kernel that owns key blocks (dK, dV written
+ * once; dQ accumulated in f32) and a dQ landing pass (scale and cast).
+ * Grouped-query attention follows the flash-linear-attention issue "Evaluate
+ * KV-head-owned GQA dKV backward" (section "Bounded scope", items 1-2): one
+ * CTA owns a key tile of one KV head and loops over the G query heads of the
+ * group.  Top-k sparse attention over a shared latent K/V row follows the
+ * tilelang pull request "Adaptive threads for sparse MLA backward".
+ *
+ * Conventions for every entry point:
+ *   - Tensors are BSHD (batch, sequence, head, head-dim) in device memory,
+ *     addressed as base + b*st.b + s*st.s + h*st.h + d (element strides; the
+ *     head-dim stride is 1).  Base pointers and the strides b, s, h (in bytes)
+ *     must be 16-byte aligned.  16-bit tensors hold ATTN_DT_F16 or
+ *     ATTN_DT_BF16 values as given by ``dtype``.
+ *   - The caller owns every buffer, including the workspace; the library
+ *     allocates nothing and keeps no state between calls.  Calls on different
+ *     streams are independent as long as each uses its own workspace.
+ *   - ``stream`` is a cudaStream_t (NULL: the legacy default stream).  All
+ *     work is asynchronous; a call returns after queueing its launches.
+ *   - A call either queues all of its launches or returns an error before
+ *     queueing any: argument errors come back as ATTN_ERR_INVALID_ARG or
+ *     ATTN_ERR_UNSUPPORTED, never as a silent fallback.  Faults found by the
+ *     kernels themselves (a bounded wait that ran out) are recorded in the
+ *     workspace and reported by attn_bwd_check_error.
+ *   - Order on one stream, same workspace: attn_bwd_preprocess, then
+ *     attn_bwd / attn_bwd_gqa (or attn_bwd_sparse), then attn_bwd_dq_land
+ *     (or attn_bwd_sparse_land).
+ */
+#ifndef ATTN_BWD_H_
+#define ATTN_BWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_BWD_API __attribute__((visibility("default")))
+#else
+#define ATTN_BWD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_DT_F16 = 0, ATTN_DT_BF16 = 1 } attn_dtype_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer or stride */
+  ATTN_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels serve (head dim, group size, ...) */
+  ATTN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than attn_bwd_workspace_size() */
+  ATTN_ERR_LAUNCH = 4,      /* the CUDA runtime refused a launch */
+  ATTN_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (reported by attn_bwd_check_error) */
+  ATTN_ERR_DEVICE = 6       /* a CUDA error surfaced while synchronising */
+} attn_status_t;
+
+/* Element strides of a BSHD tensor (or b, h, s strides of an LSE [B,H,S]). */
+typedef struct {
+  int64_t b, s, h;
+} attn_strides_t;
+
+/* Which keys a query sees, within one sequence.  Sequences: each batch row,
+ * or, when cu_seqlens is given (B must be 1), the packed ranges
+ * [cu_seqlens[n], cu_seqlens[n+1]) along S.  Positions are local to a
+ * sequence.  Query i sees key j iff
+ *   causal == 0 and window_left < 0 : always,
+ *   causal != 0                     : j <= i  (the page's "cols <= rows"),
+ *   window_left = W > 0             : i - W < j <= i  (implies causal).
+ * cu_seqlens: device int32 [num_seqs + 1], non-decreasing from 0 and ending
+ * at most at S (the kernels clamp to S); NULL for dense batches. */
+typedef struct {
+  int32_t causal;
+  int32_t window_left;
+  const int32_t* cu_seqlens;
+  int32_t num_seqs;
+} attn_mask_t;
+
+/* Bytes of workspace one backward call needs: a 256-byte header (device error
+ * word, tile counter), LSE*log2(e) and delta as f32 [B,H,S], the f32 dQ
+ * accumulator [B,S,H,Dq], and ``dkv_elems`` f32 for a sparse dKV accumulator
+ * (0 for dense).  Every region is 256-byte aligned. */
+ATTN_BWD_API size_t attn_bwd_workspace_size(int64_t B, int64_t S, int64_t H, int64_t Dq, int64_t dkv_elems);
+
+/* Launch 1: delta_i = sum_d O_id dO_id (f32), LSE*log2(e), zeroed dQ (and
+ * dKV) accumulators, cleared error word and tile counter.  The delta row
+ * preprocess of the TileOPs page ("delta_rows" in its Base and Tiled
+ * programs).
+ *   o, dO : [B,S,H,Dv] 16-bit;  lse : f32, lse[b*slse.b + h*slse.h + s*slse.s]
+ *   Dq    : head dim of Q (sizes the dQ accumulator); dkv_elems as above.
+ * Dv must be a multiple of 8 and at most 1024. */
+ATTN_BWD_API attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                                  const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t H,
+                                  int64_t Dv, int64_t Dq, int64_t dkv_elems, attn_dtype_t dtype, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* Launch 2, grouped-query attention: one CTA per (key tile of 128 rows,
+ * KV head, batch) keeps K and V in shared memory and dK, dV in tensor memory,
+ * loops over the G = HQ/HKV query heads of its group and their query blocks,
+ * writes dK (times sm_scale) and dV once in the input dtype and adds its dQ
+ * partials into the workspace accumulator.  Query head h reads KV head h / G.
+ *   q, dO  : [B,S,HQ,D] 16-bit;  k, v, dk, dv : [B,S,HKV,D] 16-bit (dk, dv written)
+ *   D in {64, 128};  G in {1, 2, 4, 8, 16};  S >= 1;  B == 1 when varlen. */
+ATTN_BWD_API attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                           attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S,
+                           int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
+                           const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Launch 2, multi-head attention: attn_bwd_gqa with HQ == HKV == H (the
+ * page's MHA op is GQA with H_kv = H). */
+ATTN_BWD_API attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                       attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S, int64_t H,
+                       int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dk,
+                       attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Launch 3: dQ = cast(sm_scale * dQacc), the TileOPs page's "dq_land".
+ *   dq : [B,S,H,D] 16-bit (written). */
+ATTN_BWD_API attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
+                               attn_dtype_t dtype, float sm_scale, const void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Launch 2, top-k sparse attention over shared latent rows (the tilelang
+ * sparse MLA backward): query t of batch b, head h (KV head g = h / (H/HKV))
+ * attends the latent rows kv[b, idx[b,t,g,s], g, :] for every slot s whose
+ * index lies in [0, SKV) (-1 pads).  K is the whole DQK-wide row, V its first
+ * DV columns.  Adds dQ partials into the workspace dQ accumulator and
+ * dKV = dK + [dV, 0] partials into the workspace dKV accumulator
+ * (dkv_elems = B*SKV*HKV*DQK at preprocess time).
+ *   q : [B,S,H,DQK];  kv : [B,SKV,HKV,DQK];  dO : [B,S,H,DV] 16-bit
+ *   idx : int32 [B,S,HKV,topk] with strides sidx (slot stride 1)
+ *   DQK = 576, DV = 512;  H / HKV a multiple of 64;  topk a multiple of 64. */
+ATTN_BWD_API attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
+                              const void* dO, attn_strides_t sdo, const int32_t* idx, attn_strides_t sidx,
+                              int64_t B, int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV,
+                              int64_t topk, attn_dtype_t dtype, float sm_scale, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Launch 3 of the sparse path: dQ = cast(dQacc) and dKV = cast(dKVacc).
+ * (The sparse kernel applies sm_scale to dS itself: dKV mixes the scaled dK
+ * term with the unscaled dV term, so the scale cannot be folded into the
+ * landing pass as on the dense path.)
+ *   dq : [B,S,H,DQK];  dkv : [B,SKV,HKV,DQK] 16-bit (written). */
+ATTN_BWD_API attn_status_t attn_bwd_sparse_land(void* dq, attn_strides_t sdq, void* dkv, attn_strides_t sdkv, int64_t B,
+                                   int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK,
+                                   attn_dtype_t dtype, const void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Synchronises ``stream`` and reports the device error word of ``workspace``:
+ * ATTN_OK, ATTN_ERR_TIMEOUT (a bounded wait ran out; *device_code, if not
+ * NULL, receives the site code) or ATTN_ERR_DEVICE (a CUDA error). */
+ATTN_BWD_API attn_status_t attn_bwd_check_error(const void* workspace, void* stream, int32_t* device_code);
+
+/* Static description of a status code. */
+ATTN_BWD_API const char* attn_bwd_status_string(attn_status_t status);
+
+/* Host-side schedule helper, exported so that the tile/mask derivation can be
+ * checked against a brute-force mask: the half-open range [*lo, *hi) of query
+ * blocks of ``block_q`` rows that a key tile [k0, k0 + block_k) of a sequence
+ * of ``len`` positions must visit so that no visible (query, key) pair is
+ * missed and no block without one is visited. */
+ATTN_BWD_API void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_t len, int32_t causal, int32_t window_left,
+                                int32_t block_q, int32_t* lo, int32_t* hi);
+
+/* Self-test of the bounded-wait machinery: launches one CTA that waits on a
+ * barrier nothing signals, with a ``timeout_us`` limit, and returns what
+ * attn_bwd_check_error then reports (ATTN_ERR_TIMEOUT when the machinery
+ * works).  Needs a workspace of at least 256 bytes. */
+ATTN_BWD_API attn_status_t attn_bwd_selftest_timeout(void* workspace, size_t workspace_bytes, int32_t timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_BWD_H_ */
