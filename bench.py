@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention backward on GB300.
+
+One step = one full backward (preprocess, main kernel, dQ landing: every
+launch of the path) over one batch of the causal MHA workload
+B=2, S=2048, H=32, D=128, fp16 (the "llama-8b-long" row of the TileOPs MHA
+backward page's performance table), inputs resident in HBM.  The metric is
+TFLOP/s with the causal convention 2.5 x the causal forward = 5*B*H*S^2*D.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead, on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own copy of the workload (independent
+batches, no collective in the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn-bwd TFLOP/s (dQ,dK,dV) & % of GB300 fp16/bf16 tensor peak; sparse: HBM GB/s"
+MAIN_WORKLOAD = "mha_causal_2x2048x32x128_f16"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dense_flops(w) -> float:
+    """2.5 x forward; forward = 4*S_q*S_k*D per head, halved when causal; for
+    packed varlen/window: 4*D per attended (query, key) pair."""
+    if w.cu_seqlens is not None or w.window > 0:
+        pairs = 0
+        for a, e in zip(w.cu_seqlens[:-1], w.cu_seqlens[1:]):
+            n = e - a
+            for i in range(n):
+                lo = max(0, i - w.window + 1) if w.window > 0 else 0
+                pairs += i - lo + 1
+        return 2.5 * 4.0 * w.D * pairs * w.HQ * w.B
+    f = 4.0 * w.B * w.HQ * w.S * w.S * w.D
+    return 2.5 * (f / 2 if w.causal else f)
+
+
+def sparse_flops(w, idx) -> float:
+    """Per valid (token, slot) pair and head: S (2*DQK), dP (2*DV), dV (2*DV),
+    dK (2*DQK), dQ (2*DQK)."""
+    valid = int(((idx >= 0) & (idx < w.S)).sum())
+    return valid * w.HQ * 2.0 * (3 * w.D + 2 * w.Dv)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel_src: str, name: str):
+    """DRAM bytes per launch of ``name`` from the committed ncu summary, only if
+    it was taken on the current kernel source (matching hash)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(name)
+    if not rec:
+        return None
+    with open(kernel_src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec.get("dram_bytes_per_launch") if rec.get("source_sha256_16") == h else None
+
+
+# ------------------------------------------------------------------ inputs (GPU arm)
+
+def gpu_dense_inputs(w, device):
+    """Q, K, V, dO from the seeded generator; O and LSE from a float32 torch
+    forward on the device (input preparation only; it is not timed)."""
+    import torch
+
+    from attention_backward_gb300 import inputs
+
+    q, k, v, do = inputs.dense_inputs(w)
+    tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    tq, tk, tv, tdo = (torch.from_numpy(a).to(device).to(tdt) for a in (q, k, v, do))
+    G = w.HQ // w.HKV
+    o = torch.empty_like(tdo)
+    lse = torch.empty(w.B, w.HQ, w.S, dtype=torch.float32, device=device)
+    seqs = [(0, w.S)] if w.cu_seqlens is None else list(zip(w.cu_seqlens[:-1], w.cu_seqlens[1:]))
+    for b in range(w.B):
+        for (a, e) in seqs:
+            n = e - a
+            i = torch.arange(n, device=device)[:, None]
+            j = torch.arange(n, device=device)[None, :]
+            vis = torch.ones(n, n, dtype=torch.bool, device=device)
+            if w.causal or w.window > 0:
+                vis &= j <= i
+            if w.window > 0:
+                vis &= j > i - w.window
+            for h in range(w.HQ):
+                Q = tq[b, a:e, h].float()
+                K = tk[b, a:e, h // G].float()
+                V = tv[b, a:e, h // G].float()
+                s = (Q @ K.T) * w.sm_scale
+                s = s.masked_fill(~vis, float("-inf"))
+                l = torch.logsumexp(s, dim=1)
+                o[b, a:e, h] = (torch.exp(s - l[:, None]) @ V).to(tdt)
+                lse[b, h, a:e] = l
+    return tq, tk, tv, o, tdo, lse
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def time_dense(w, steps, warmup, device, flush_bytes=256 << 20):
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    tq, tk, tv, to, tdo, lse = gpu_dense_inputs(w, device)
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=device) if w.cu_seqlens else None
+    ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
+    dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        ab.preprocess(to, tdo, lse, ws, Dq=w.D, stream=stream)
+        ev[1].record(stream)
+        ab.attn_bwd_gqa(tq, tk, tv, tdo, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
+        ev[2].record(stream)
+        ab.dq_land(dq, ws, w.sm_scale, stream)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(warmup):
+        flush.zero_()
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+    ab.check_error(ws, stream)
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(steps):
+        flush.zero_()  # L2 flush between timed steps (256 MiB write > 129 MB L2)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+        per.append(ev)
+    torch.cuda.synchronize(device)
+    ab.check_error(ws, stream)
+    tot = [e[0].elapsed_time(e[3]) for e in per]
+    pre = [e[0].elapsed_time(e[1]) for e in per]
+    main = [e[1].elapsed_time(e[2]) for e in per]
+    land = [e[2].elapsed_time(e[3]) for e in per]
+    return {"ms_step": float(np.mean(tot)), "ms_pre": float(np.mean(pre)), "ms_main": float(np.mean(main)),
+            "ms_land": float(np.mean(land)), "ms_step_median": float(np.median(tot)),
+            "tensors": (tq, tk, tv, to, tdo, lse, cu)}
+
+
+def time_e2e(w, tensors, steps, device):
+    """The same backward through the public API with pinned host buffers:
+    host->device copies of the inputs and device->host copies of dQ, dK, dV
+    inside the timed region."""
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    tq, tk, tv, to, tdo, lse, cu = tensors
+    host_in = [t.cpu().pin_memory() for t in (tq, tk, tv, to, tdo, lse)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (tq, tk, tv)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream(device)
+    ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
+    dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_in]
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        dq, dk, dv = ab.backward(*dev_in, w.sm_scale, causal=w.causal, window=w.window, cu_seqlens=cu,
+                                 workspace=ws, stream=stream)
+        for h, d in zip(host_out, (dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def cpu_oracle_sample(w, budget_s=12.0):
+    """The oracle backward timed on the host cores over a bounded sample of the
+    workload (a prefix of the query heads, all batch rows); inputs from the
+    seeded generator and the oracle's own forward (not timed)."""
+    import oracle
+    from attention_backward_gb300 import inputs
+
+    q, k, v, do = inputs.dense_inputs(w)
+    mask = dict(causal=w.causal, window=w.window, cu_seqlens=w.cu_seqlens)
+    # calibrate on one head, then time as many heads as fit the budget
+    o1, l1 = oracle.forward(q[:, :, :1], k[:, :, :1], v[:, :, :1], w.sm_scale, **mask)
+    o1 = inputs.round_to_dtype(o1, w.dtype)
+    t0 = time.perf_counter()
+    oracle.backward(q[:, :, :1], k[:, :, :1], v[:, :, :1], o1, do[:, :, :1], l1, w.sm_scale, **mask)
+    t1 = time.perf_counter() - t0
+    nh = int(max(1, min(w.HQ, budget_s // max(t1, 1e-3))))
+    G = w.HQ // w.HKV
+    nh = max(G, (nh // G) * G)
+    qs, ks, vs, dos = q[:, :, :nh], k[:, :, :nh // G], v[:, :, :nh // G], do[:, :, :nh]
+    o, lse = oracle.forward(qs, ks, vs, w.sm_scale, **mask)
+    o = inputs.round_to_dtype(o, w.dtype)
+    t0 = time.perf_counter()
+    oracle.backward(qs, ks, vs, o, dos, lse, w.sm_scale, **mask)
+    el = time.perf_counter() - t0
+    frac = nh / w.HQ
+    return dense_flops(w) * frac / el / 1e12, el, nh
+
+
+# ------------------------------------------------------------------ main
+
+def dist_setup(n):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def run_reference(args):
+    """CPU oracle arm: each step times the oracle on a bounded sample."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from attention_backward_gb300 import inputs
+
+    w = inputs.WORKLOADS[MAIN_WORKLOAD]
+    vals, els = [], []
+    for i in range(args.warmup + args.steps):
+        v_, el, nh = cpu_oracle_sample(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+        if i >= args.warmup:
+            vals.append(v_)
+            els.append(el)
+    value = float(np.mean(vals))
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(els)) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": MAIN_WORKLOAD, "B": w.B, "S": w.S, "H": w.HQ, "D": w.D, "causal": True},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{nh} of {w.HQ} query heads, both batch rows, per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import __graft_entry__
+
+    world, rank, local = dist_setup(args.gpus)
+    __graft_entry__.build()
+    from attention_backward_gb300 import inputs
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = inputs.WORKLOADS[MAIN_WORKLOAD]
+    pk, pk_kind = peaks()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    r = time_dense(w, args.steps, args.warmup, device)
+    clk = clocks.stop()
+    ms = r["ms_step"]
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms, r["ms_main"]], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_main = float(t[0]), float(t[1])
+    else:
+        ms_main = r["ms_main"]
+    flops = dense_flops(w)
+    value = flops * world / (ms * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e(w, r["tensors"], max(3, args.steps // 4), device)
+    peak = float(pk["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
+    achieved = flops / (ms_main * 1e-3) / 1e12
+    traffic = traffic_record(os.path.join(ROOT, "attention_backward_gb300", "csrc", "dense_bwd.cu"),
+                             "dense_bwd_kernel<128,f16>@" + MAIN_WORKLOAD)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": MAIN_WORKLOAD, "B": w.B, "S": w.S, "H": w.HQ, "D": w.D, "causal": True,
+                   "sm_scale": w.sm_scale, "l2": "flushed before every step (256 MiB write)",
+                   "timed": "preprocess + main + dQ landing per step"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": f"bf16 burst, {pk_kind}",
+                     "kernel": "dense_bwd_kernel<128,f16>", "kernel_ms": ms_main},
+        "stages_ms": {"preprocess": r["ms_pre"], "main": r["ms_main"], "dq_land": r["ms_land"]},
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    del r
+    if not args.no_extra and world == 1:
+        line["workloads"] = extra_workloads(max(5, args.steps // 2), args.warmup, device, pk)
+    if not args.no_cpu and world == 1 and rank == 0:
+        cv, el, nh = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": cv, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{nh} of {w.HQ} query heads x {w.B} batch rows of {MAIN_WORKLOAD}, "
+                                          f"{el:.1f} s of float64 numpy"}
+    else:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def extra_workloads(steps, warmup, device, pk):
+    """The other dense workloads, same timing method (context for the roofline)."""
+    import torch
+
+    from attention_backward_gb300 import inputs
+
+    out = {}
+    for name in ("gqa_1x16384_hq32_hkv4_d128_bf16", "gqa_varlen_window1024_hq32_hkv8_d64_bf16"):
+        w = inputs.WORKLOADS[name]
+        r = time_dense(w, steps, warmup, device)
+        f = dense_flops(w)
+        out[name] = {"ms_per_step": r["ms_step"], "TFLOP/s": f / (r["ms_step"] * 1e-3) / 1e12,
+                     "main_ms": r["ms_main"], "main_frac_of_peak": f / (r["ms_main"] * 1e-3) / 1e12 / pk["bf16_tflops"]}
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())
