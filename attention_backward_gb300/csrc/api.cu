@@ -67,6 +67,22 @@ bool make_map(CUtensorMap* m, const void* base, attn_dtype_t dt, int64_t B, int6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// f32 accumulator [B,S,H,D] (contiguous) as the target of bulk reduce-adds:
+// box (box_d, 1, rows, 1); 128-byte swizzle when box_d * 4 == 128.
+bool make_acc_map(CUtensorMap* m, void* base, int64_t B, int64_t S, int64_t H, int64_t D, int box_d, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 4), static_cast<cuuint64_t>(H * D * 4),
+                           static_cast<cuuint64_t>(S * H * D * 4)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d), 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = box_d * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uint64_t wait_limit_ns() { return ab::kWaitTimeoutNs; }
 
 }  // namespace
@@ -164,6 +180,8 @@ attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn
       !make_map(&m.k, k, dtype, B, S, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, S, HKV, D, sv, kDenseBM))
     return ATTN_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // dQ partials: D = 128 lands 64-query x 128-d boxes, D = 64 lands 128-query x 32-d swizzled boxes
+  if (!make_acc_map(&m.dq, ws + L.dq_off, B, S, HQ, D, D == 128 ? 128 : 32, BN)) return ATTN_ERR_INVALID_ARG;
   DenseParams p{};
   p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV);
   p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D);
@@ -177,10 +195,12 @@ attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn
   p.dk = static_cast<uint8_t*>(dk), p.sdk_b = sdk.b, p.sdk_s = sdk.s, p.sdk_h = sdk.h;
   p.dv = static_cast<uint8_t*>(dv), p.sdv_b = sdv.b, p.sdv_s = sdv.s, p.sdv_h = sdv.h;
   p.timeout_ns = wait_limit_ns();
-  // key tiles per (batch, KV head): a packed batch may add one partial tile per sequence
-  const int64_t tiles = (S + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0);
-  const int64_t grid = tiles * B * HKV;
-  if (grid >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  p.tile_counter = &reinterpret_cast<WsHeader*>(ws)->tile_counter;
+  // key tiles per (batch, KV head): a packed batch may add one partial tile per
+  // sequence.  Persistent CTAs, one per SM, draw tiles from the counter.
+  const int64_t tiles = ((S + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0)) * B * HKV;
+  if (tiles >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  const int64_t grid = tiles < sm_count() ? tiles : sm_count();
   return launch_status(launch_dense(p, m, dtype == ATTN_DT_BF16, static_cast<int>(grid),
                                     static_cast<cudaStream_t>(stream)));
 }

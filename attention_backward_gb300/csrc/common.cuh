@@ -47,10 +47,14 @@ enum DeviceError : int {
   kErrWaitDP = 0x107,
   kErrWaitDS = 0x108,
   kErrWaitDSFree = 0x109,
-  kErrWaitPFree = 0x10A,
+  kErrWaitSFree = 0x10A,
   kErrWaitDQFull = 0x10B,
   kErrWaitDQEmpty = 0x10C,
   kErrWaitDKV = 0x10D,
+  kErrWaitTile = 0x10E,
+  kErrWaitKVFree = 0x10F,
+  kErrWaitStage = 0x110,
+  kErrWaitDKVFree = 0x111,
   kErrSelftest = 0x1FF,
   kErrSparseBase = 0x200,
 };

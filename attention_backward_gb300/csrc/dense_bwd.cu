@@ -1,33 +1,43 @@
-// Launch 2 of the dense backward: the key-block-owned main kernel.
+// Launch 2 of the dense backward: the persistent, key-block-owned main kernel.
 //
 // Structure (the "Tiled" placement of the TileOPs MHA backward page, section
 // "TileFoundry Description", re-designed for the 5th-generation tensor core):
-// one CTA owns a key tile of BM = 128 rows of one KV head (and batch row or
+// a tile is a block of BM = 128 key rows of one KV head (and batch row or
 // packed sequence).  K and V stay in shared memory, dK and dV accumulate in
 // tensor memory (TMEM) over every query block of every query head of the
 // group (KV-head ownership, flash-linear-attention issue "Evaluate
-// KV-head-owned GQA dKV backward", "Bounded scope" items 1-2), and are
-// written once, in the input dtype, at the end.  Per query block of BN rows:
+// KV-head-owned GQA dKV backward", "Bounded scope" items 1-2), and are written
+// once, in the input dtype, when the tile ends.  Per step (one query block of
+// BN rows of one query head):
 //
-//   S^T  = K Q^T                   (tcgen05, M=128 keys, N=BN, K=D)
-//   P^T  = exp2(S^T*scale*log2e - LSE2)  masked; rounded to 16 bit into TMEM
-//   dP^T = V dO^T                  (tcgen05)
-//   dV  += P^T dO                  (A = P^T from TMEM)
+//   S^T  = K Q^T                   tensor core, M = 128 keys, N = BN, K = D
+//   P^T  = exp2(S^T*scale*log2e - LSE2)  masked, rounded to 16 bits, back into TMEM
+//   dP^T = V dO^T                  tensor core
+//   dV  += P^T dO                  A operand = P^T from TMEM
 //   dS^T = P^T o (dP^T - delta)    unscaled (the page folds the scale into dK and dQ)
-//   dK  += dS^T Q                  (A = dS^T from TMEM)
-//   dQ  partial = dS K             (A/B from shared memory), added in f32 to the
-//                                   workspace accumulator by atomics
+//   dK  += dS^T Q                  A operand = dS^T from TMEM
+//   dQ   = dS K                    from shared memory; added into the f32 workspace
+//                                  accumulator with one bulk tensor reduce-add
 //
 // D = 128 uses BN = 64 and computes dQ^T = K^T dS^T (M = 128 head dims);
 // D = 64 uses BN = 128 and computes dQ = dS K (M = 128 queries).
 //
-// Warp roles (14 warps): 0-3 dQ epilogue (TMEM -> global f32 atomics),
+// Pipelining: S^T is double-buffered in TMEM and the S^T of step i+1 is
+// issued before dV/dK/dQ of step i, so the softmax of one step overlaps the
+// tensor work of the previous one.  P^T and dS^T of a step are written over
+// that step's S^T columns.  Q/dO come through a 3-stage TMA ring.  A stage is
+// released only by a tensor-core commit issued after every MMA reading it,
+// and no accumulator is read before its commit completed (the two pipelining
+// faults the TileOPs page reports fixing in its older kernel, "Summary").
+//
+// Persistent CTAs (one per SM) draw tiles, longest first, from a counter in
+// the workspace that the preprocess zeroes; each CTA's producer publishes the
+// tile to the other roles through a two-slot ring in shared memory.
+//
+// Warp roles (14 warps): 0-3 dQ epilogue (TMEM -> shared -> bulk reduce),
 // 4-11 two warpgroups of softmax/dS work (each owns half of the BN query
-// columns of all 128 key rows), 12 TMA producer, 13 MMA issuer (one thread).
-// A Q/dO stage is released only by a tensor-core commit issued after every
-// MMA that reads it; an accumulator is read only after its commit completed
-// (the two pipelining faults the TileOPs page reports fixing in its older
-// kernel, "Summary").
+// columns of all 128 key rows) that also land dK/dV, 12 TMA producer,
+// 13 MMA issuer (one thread).  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -44,117 +54,148 @@ template <int D>
 struct Cfg {
   static constexpr int BM = kDenseBM;
   static constexpr int BN = dense_bn(D);
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 3;
   static constexpr int NSLAB = D / 64;  // 64-column (128-byte) slabs per row
   static constexpr int KV_SLAB = BM * 128;
   static constexpr int KV_TILE = KV_SLAB * NSLAB;
   static constexpr int Q_SLAB = BN * 128;
   static constexpr int Q_TILE = Q_SLAB * NSLAB;
   static constexpr int DS_BYTES = BM * BN * 2;
+  static constexpr int STG_BYTES = BN * D * 4;  // f32 dQ staging of one step
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_TILE;
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
+  static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
   static constexpr int OFF_DELTA = OFF_LSE + STAGES * BN * 4;
-  static constexpr int OFF_BAR = OFF_DELTA + STAGES * BN * 4;
-  static constexpr int NBAR = 2 * STAGES + 16;
+  static constexpr int OFF_RING = OFF_DELTA + STAGES * BN * 4;
+  static constexpr int OFF_BAR = OFF_RING + 64;
+  static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
-  // tensor memory columns (512 allocated)
-  static constexpr int T_S = 0;                // S^T f32 [128 x BN]; P^T 16-bit pairs overwrite its first BN/2 columns
-  static constexpr int T_DP = BN;              // dP^T f32 [128 x BN]
-  static constexpr int T_DV = 2 * BN;          // dV f32 [128 x D]
-  static constexpr int T_DK = 2 * BN + D;      // dK f32 [128 x D]
-  static constexpr int T_DQ = 2 * BN + 2 * D;  // dQ^T [128 d x 64 q] (D=128) or dQ [128 q x 64 d] (D=64)
-  static constexpr int T_DS = T_DQ + 64;       // dS^T 16-bit pairs [128 x BN/2]
-  static_assert(T_DS + BN / 2 <= 512, "TMEM budget");
-  static constexpr int THREADS = 14 * 32;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // tensor memory columns (512 allocated)
+  static constexpr int T_SB = 0;           // two S^T buffers [128 x BN] f32; P^T / dS^T (16-bit pairs) overwrite them
+  static constexpr int T_DP = 2 * BN;      // dP^T f32 [128 x BN]
+  static constexpr int T_DV = 3 * BN;      // dV f32 [128 x D]
+  static constexpr int T_DK = 3 * BN + D;  // dK f32 [128 x D]
+  // dQ^T [128 d x 64 q] in its own columns (D = 128); dQ [128 q x 64 d] over dP^T (D = 64)
+  static constexpr int T_DQ = D == 128 ? 3 * BN + 2 * D : T_DP;
+  static_assert(3 * BN + 2 * D + (D == 128 ? 64 : 0) <= 512, "TMEM budget");
+  static constexpr int THREADS = 14 * 32;
 };
 
 enum Bar : int {
-  B_FULL = 0,  // + stage
-  B_EMPTY = 2, // + stage (STAGES == 2)
-  B_KV = 4,
-  B_S,
-  B_DP,
-  B_SREAD,
-  B_P,
-  B_DS,
-  B_PFREE,
-  B_DSFREE,
-  B_DQFULL,
-  B_DQEMPTY,
-  B_DKV,
-  B_DRAIN,
+  FULL0 = 0,   // 3 stages
+  EMPTY0 = 3,  // 3 stages
+  KV_FULL = 6,
+  KV_FREE,
+  TILE_FULL0,       // 2 slots
+  TILE_EMPTY0 = 10, // 2 slots
+  S_FULL0 = 12,     // 2 buffers
+  S_FREE0 = 14,     // 2 buffers
+  SREAD = 16,
+  P_READY,
+  DP_FULL,
+  DS_READY,
+  DS_SFREE,
+  DQ_FULL,
+  DQ_EMPTY,
+  STG_FREE,
+  STG_FULL,
+  DKV_FULL,
+  DKV_FREE,
+  DRAIN,
+  NUM_BARS
 };
 
+struct TileInfo {
+  int b, g, seq_start, len, k0, qlo, nq, valid;
+};
+
+// Tile t -> (batch, KV head, key block); longest tiles first (smallest key
+// block index first, which is the longest under a causal mask).
+__device__ TileInfo decode_tile(int t, const DenseParams& p) {
+  TileInfo ti{};
+  ti.valid = 0;
+  const int BH = p.B * p.HKV;
+  if (t < 0) return ti;
+  const int bh = t % BH;
+  int r = t / BH;
+  ti.b = bh / p.HKV;
+  ti.g = bh % p.HKV;
+  if (p.cu_seqlens != nullptr) {
+    bool found = false;
+    for (int n = 0; n < p.num_seqs; ++n) {
+      const int a = clamp_pos(p.cu_seqlens[n], p.S), e = clamp_pos(p.cu_seqlens[n + 1], p.S);
+      const int nt = e > a ? (e - a + kDenseBM - 1) / kDenseBM : 0;
+      if (r < nt) {
+        ti.seq_start = a;
+        ti.len = e - a;
+        found = true;
+        break;
+      }
+      r -= nt;
+    }
+    if (!found) return ti;
+  } else {
+    if (static_cast<int64_t>(r) * kDenseBM >= p.S) return ti;
+    ti.seq_start = 0;
+    ti.len = p.S;
+  }
+  ti.k0 = r * kDenseBM;
+  int lo, hi;
+  query_block_range(ti.k0, kDenseBM, ti.len, p.causal, p.window, dense_bn(p.D), &lo, &hi);
+  ti.qlo = lo;
+  ti.nq = hi - lo;
+  ti.valid = 1;
+  return ti;
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
-    dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
   using C = Cfg<D>;
-  constexpr int BM = C::BM, BN = C::BN, STAGES = C::STAGES;
-  static_assert(STAGES == 2, "barrier enum assumes two stages");
+  constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  TileInfo* ring = reinterpret_cast<TileInfo*>(sm + C::OFF_RING);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
   float* s_lse = reinterpret_cast<float*>(sm + C::OFF_LSE);
   float* s_delta = reinterpret_cast<float*>(sm + C::OFF_DELTA);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---------------------------------------------------------------- tile
-  const int BH = p.B * p.HKV;
-  const int bh = blockIdx.x % BH;
-  int t = blockIdx.x / BH;
-  const int b = bh / p.HKV, g = bh % p.HKV;
-  int seq_start = 0, len = p.S;
-  if (p.cu_seqlens != nullptr) {
-    bool found = false;
-    for (int n = 0; n < p.num_seqs; ++n) {
-      const int a = clamp_pos(p.cu_seqlens[n], p.S), e = clamp_pos(p.cu_seqlens[n + 1], p.S);
-      const int nt = e > a ? (e - a + BM - 1) / BM : 0;
-      if (t < nt) {
-        seq_start = a;
-        len = e - a;
-        found = true;
-        break;
-      }
-      t -= nt;
-    }
-    if (!found) return;
-  } else if (t * BM >= p.S) {
-    return;
-  }
-  const int k0 = t * BM;
-  int qlo, qhi;
-  query_block_range(k0, BM, len, p.causal, p.window, BN, &qlo, &qhi);
-  const int nq = qhi - qlo;
-  const int n_steps = p.G * nq;
-
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&bars[B_FULL + i], 2);
-      mbar_init(&bars[B_EMPTY + i], 1);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&bars[FULL0 + i], 2);  // producer: expect_tx arrival + arrival after LSE/delta stores
+      mbar_init(&bars[EMPTY0 + i], 1);
     }
-    mbar_init(&bars[B_KV], 1);
-    mbar_init(&bars[B_S], 1);
-    mbar_init(&bars[B_DP], 1);
-    mbar_init(&bars[B_SREAD], 8);
-    mbar_init(&bars[B_P], 8);
-    mbar_init(&bars[B_DS], 8);
-    mbar_init(&bars[B_PFREE], 1);
-    mbar_init(&bars[B_DSFREE], 1);
-    mbar_init(&bars[B_DQFULL], 1);
-    mbar_init(&bars[B_DQEMPTY], 4);
-    mbar_init(&bars[B_DKV], 1);
-    mbar_init(&bars[B_DRAIN], 1);
+    mbar_init(&bars[KV_FULL], 1);
+    mbar_init(&bars[KV_FREE], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[TILE_FULL0 + i], 1);
+      mbar_init(&bars[TILE_EMPTY0 + i], 13);  // MMA thread + 8 compute warps + 4 epilogue warps
+      mbar_init(&bars[S_FULL0 + i], 1);
+      mbar_init(&bars[S_FREE0 + i], 1);
+    }
+    mbar_init(&bars[SREAD], 8);
+    mbar_init(&bars[P_READY], 8);
+    mbar_init(&bars[DP_FULL], 1);
+    mbar_init(&bars[DS_READY], 8);
+    mbar_init(&bars[DS_SFREE], 1);
+    mbar_init(&bars[DQ_FULL], 1);
+    mbar_init(&bars[DQ_EMPTY], 4);
+    mbar_init(&bars[STG_FREE], 1);
+    mbar_init(&bars[STG_FULL], 4);
+    mbar_init(&bars[DKV_FULL], 1);
+    mbar_init(&bars[DKV_FREE], 8);
+    mbar_init(&bars[DRAIN], 1);
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -169,54 +210,76 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
   if (warp == 12) {
     // ============================================================ producer
-    int pending[STAGES];
+    int pend_full[ST];
 #pragma unroll
-    for (int i = 0; i < STAGES; ++i) pending[i] = -1;
-    if (lane == 0) {
-      tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.dO);
-      mbar_arrive_expect_tx(&bars[B_KV], 2 * C::KV_TILE);
-#pragma unroll
-      for (int s = 0; s < C::NSLAB; ++s) {
-        tma_load_4d(sm + C::OFF_K + s * C::KV_SLAB, &maps.k, &bars[B_KV], s * 64, g, seq_start + k0, b);
-        tma_load_4d(sm + C::OFF_V + s * C::KV_SLAB, &maps.v, &bars[B_KV], s * 64, g, seq_start + k0, b);
-      }
-    }
-    for (int i = 0; i < n_steps; ++i) {
-      const int st = i % STAGES, r = i / STAGES;
-      if (i >= STAGES && !mbar_wait_warp(&bars[B_EMPTY + st], (r - 1) & 1, wc, kErrWaitStageEmpty)) break;
-      const int h = g * p.G + i / nq, q0 = (qlo + i % nq) * BN;
-      const int64_t rowbase = (static_cast<int64_t>(b) * p.HQ + h) * p.S + seq_start;
-      for (int c = lane; c < BN; c += 32) {
-        const int q = q0 + c;
-        float l = 0.f, d = 0.f;
-        if (q < len) {
-          l = p.lse2[rowbase + q];
-          d = p.delta[rowbase + q];
-        }
-        s_lse[st * BN + c] = l;
-        s_delta[st * BN + c] = d;
-      }
-      __syncwarp();
+    for (int i = 0; i < ST; ++i) pend_full[i] = -1;
+    int kv_pend = -1;
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (tc >= 2 && !(ok = mbar_wait_warp(&bars[TILE_EMPTY0 + slot], ((tc >> 1) - 1) & 1, wc, kErrWaitTile))) break;
+      int t = 0;
+      if (lane == 0) t = atomicAdd(p.tile_counter, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      const TileInfo ti = decode_tile(t, p);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[B_FULL + st], 2 * C::Q_TILE);
+        ring[slot] = ti;
+        mbar_arrive(&bars[TILE_FULL0 + slot]);
+      }
+      if (!ti.valid) break;
+      if (tc >= 1 && !(ok = mbar_wait_warp(&bars[KV_FREE], (tc - 1) & 1, wc, kErrWaitKVFree))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[KV_FULL], 2 * C::KV_TILE);
 #pragma unroll
         for (int s = 0; s < C::NSLAB; ++s) {
-          tma_load_4d(sm + C::OFF_Q + st * C::Q_TILE + s * C::Q_SLAB, &maps.q, &bars[B_FULL + st], s * 64, h,
-                      seq_start + q0, b);
-          tma_load_4d(sm + C::OFF_DO + st * C::Q_TILE + s * C::Q_SLAB, &maps.dO, &bars[B_FULL + st], s * 64, h,
-                      seq_start + q0, b);
+          tma_load_4d(sm + C::OFF_K + s * C::KV_SLAB, &maps.k, &bars[KV_FULL], s * 64, ti.g, ti.seq_start + ti.k0,
+                      ti.b);
+          tma_load_4d(sm + C::OFF_V + s * C::KV_SLAB, &maps.v, &bars[KV_FULL], s * 64, ti.g, ti.seq_start + ti.k0,
+                      ti.b);
         }
-        mbar_arrive(&bars[B_FULL + st]);
       }
-      pending[st] = r & 1;
-    }
-    // loads still in flight must land before the CTA exits
-    if (lane == 0) {
-      mbar_drain(&bars[B_KV], 0);
+      kv_pend = tc & 1;
+      const int n = p.G * ti.nq;
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
+        const uint32_t r = gs / ST;
+        if (gs >= static_cast<uint32_t>(ST) &&
+            !(ok = mbar_wait_warp(&bars[EMPTY0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
+          break;
+        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
+        const int64_t rowbase = (static_cast<int64_t>(ti.b) * p.HQ + h) * p.S + ti.seq_start;
+        for (int c = lane; c < BN; c += 32) {
+          const int q = q0 + c;
+          float l = 0.f, d = 0.f;
+          if (q < ti.len) {
+            l = p.lse2[rowbase + q];
+            d = p.delta[rowbase + q];
+          }
+          s_lse[st * BN + c] = l;
+          s_delta[st * BN + c] = d;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[FULL0 + st], 2 * C::Q_TILE);
 #pragma unroll
-      for (int i = 0; i < STAGES; ++i)
-        if (pending[i] >= 0) mbar_drain(&bars[B_FULL + i], pending[i]);
+          for (int s = 0; s < C::NSLAB; ++s) {
+            tma_load_4d(sm + C::OFF_Q + st * C::Q_TILE + s * C::Q_SLAB, &maps.q, &bars[FULL0 + st], s * 64, h,
+                        ti.seq_start + q0, ti.b);
+            tma_load_4d(sm + C::OFF_DO + st * C::Q_TILE + s * C::Q_SLAB, &maps.dO, &bars[FULL0 + st], s * 64, h,
+                        ti.seq_start + q0, ti.b);
+          }
+          mbar_arrive(&bars[FULL0 + st]);
+        }
+        pend_full[st] = r & 1;
+      }
+    }
+    // loads still in flight land before the CTA exits
+    if (lane == 0) {
+      if (kv_pend >= 0) mbar_drain(&bars[KV_FULL], kv_pend);
+#pragma unroll
+      for (int i = 0; i < ST; ++i)
+        if (pend_full[i] >= 0) mbar_drain(&bars[FULL0 + i], pend_full[i]);
     }
   } else if (warp == 13) {
     // ============================================================ MMA issuer
@@ -227,99 +290,102 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const uint32_t sK = smem_u32(sm + C::OFF_K), sV = smem_u32(sm + C::OFF_V), sDS = smem_u32(sm + C::OFF_DS);
       auto sQ = [&](int st) { return smem_u32(sm + C::OFF_Q + st * C::Q_TILE); };
       auto sDO = [&](int st) { return smem_u32(sm + C::OFF_DO + st * C::Q_TILE); };
-      // K-major operands: K-step kk of 16 elements = slab kk/4, byte offset 32*(kk%4)
-      auto issue_S = [&](int st) {
+      auto tSB = [&](uint32_t s) { return tmem + C::T_SB + (s & 1u) * BN; };
+
+      // S^T of global step s into its buffer (waits for its stage and for the
+      // buffer's previous P^T/dS^T readers).  K-major operands: K-step kk of
+      // 16 elements = slab kk/4, byte offset 32*(kk%4).
+      auto issue_S = [&](uint32_t s) -> bool {
+        if (!mbar_wait(&bars[FULL0 + s % ST], (s / ST) & 1, wc, kErrWaitStageFull)) return false;
+        if (s >= 2 && !mbar_wait(&bars[S_FREE0 + (s & 1)], ((s - 2) >> 1) & 1, wc, kErrWaitSFree)) return false;
+        tc_fence_after();
+        const uint32_t q = sQ(s % ST);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk / 4) * C::KV_SLAB + (kk % 4) * 32, qo = (kk / 4) * C::Q_SLAB + (kk % 4) * 32;
-          mma_ss(tmem + C::T_S, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(sQ(st) + qo, 16, 1024), IDESC_S, kk > 0);
+          mma_ss(tSB(s), sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(q + qo, 16, 1024), IDESC_S, kk > 0);
         }
+        mma_commit(&bars[S_FULL0 + (s & 1)]);
+        return true;
       };
-      auto issue_dP = [&](int st) {
+      // dP^T of step s (its stage is known full: issue_S(s) waited for it).
+      auto issue_dP = [&](uint32_t s) -> bool {
+        if (D == 64 && s >= 1) {  // dQ of step s-1 lives in the dP^T columns until the epilogue read it
+          if (!mbar_wait(&bars[DQ_EMPTY], (s - 1) & 1, wc, kErrWaitDQEmpty)) return false;
+          tc_fence_after();
+        }
+        const uint32_t o = sDO(s % ST);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk / 4) * C::KV_SLAB + (kk % 4) * 32, qo = (kk / 4) * C::Q_SLAB + (kk % 4) * 32;
-          mma_ss(tmem + C::T_DP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(sDO(st) + qo, 16, 1024), IDESC_S,
-                 kk > 0);
+          mma_ss(tmem + C::T_DP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(o + qo, 16, 1024), IDESC_S, kk > 0);
         }
-      };
-      // MN-major B (dO or Q as [N = D] x [K = queries]): K-step = 16 rows = 2048 bytes
-      auto issue_dV = [&](int st, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, sdesc_sw128(sDO(st) + kk * 2048, C::Q_SLAB, 1024), IDESC_KV,
-                 acc || kk > 0);
-      };
-      auto issue_dK = [&](int st, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8, sdesc_sw128(sQ(st) + kk * 2048, C::Q_SLAB, 1024), IDESC_KV,
-                 acc || kk > 0);
-      };
-      // dQ: contraction over the 128 key rows (K-step = 16 key rows = 2048 bytes)
-      auto issue_dQ = [&]() {
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          if constexpr (D == 128)  // dQ^T = K^T dS^T: A = K tile MN-major, B = dS^T MN-major
-            mma_ss(tmem + C::T_DQ, sdesc_sw128(sK + kk * 2048, C::KV_SLAB, 1024),
-                   sdesc_sw128(sDS + kk * 2048, C::KV_SLAB, 1024), IDESC_DQ, kk > 0);
-          else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
-            mma_ss(tmem + C::T_DQ, sdesc_sw128(sDS + kk * 2048, BM * 128, 1024),
-                   sdesc_sw128(sK + kk * 2048, C::KV_SLAB, 1024), IDESC_DQ, kk > 0);
-        }
+        mma_commit(&bars[DP_FULL]);
+        return true;
       };
 
-      bool ok = mbar_wait(&bars[B_KV], 0, wc, kErrWaitKV);
-      tc_fence_after();
-      if (ok && n_steps > 0) {
-        ok = mbar_wait(&bars[B_FULL + 0], 0, wc, kErrWaitStageFull);
+      uint32_t gs = 0;
+      bool ok = true;
+      for (int tc = 0; ok; ++tc) {
+        const int slot = tc & 1;
+        if (!(ok = mbar_wait(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+        const TileInfo ti = ring[slot];
+        mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+        if (!ti.valid) break;
+        const int n = p.G * ti.nq;
+        if (!(ok = mbar_wait(&bars[KV_FULL], tc & 1, wc, kErrWaitKV))) break;
         tc_fence_after();
-        if (ok) {
-          issue_S(0);
-          mma_commit(&bars[B_S]);
-          issue_dP(0);
-          mma_commit(&bars[B_DP]);
-        }
-      }
-      for (int i = 0; ok && i < n_steps; ++i) {
-        const int st = i % STAGES;
-        if (!(ok = mbar_wait(&bars[B_P], i & 1, wc, kErrWaitP))) break;
-        tc_fence_after();
-        issue_dV(st, i > 0);
-        mma_commit(&bars[B_PFREE]);
-        if (!(ok = mbar_wait(&bars[B_DS], i & 1, wc, kErrWaitDS))) break;
-        tc_fence_after();
-        issue_dK(st, i > 0);
-        if (i > 0) {
-          if (!(ok = mbar_wait(&bars[B_DQEMPTY], (i - 1) & 1, wc, kErrWaitDQEmpty))) break;
+        if (n > 0 && (!(ok = issue_S(gs)) || !(ok = issue_dP(gs)))) break;
+        for (int j = 0; j < n; ++j, ++gs) {
+          const int st = gs % ST;
+          const uint32_t sb = tSB(gs);
+          if (j + 1 < n && !(ok = issue_S(gs + 1))) break;
+          if (!(ok = mbar_wait(&bars[P_READY], gs & 1, wc, kErrWaitP))) break;
+          if (j == 0 && tc >= 1 && !(ok = mbar_wait(&bars[DKV_FREE], (tc - 1) & 1, wc, kErrWaitDKVFree))) break;
           tc_fence_after();
-        }
-        issue_dQ();
-        mma_commit(&bars[B_DQFULL]);
-        mma_commit(&bars[B_DSFREE]);
-        mma_commit(&bars[B_EMPTY + st]);
-        if (i + 1 < n_steps) {
-          const int st1 = (i + 1) % STAGES;
-          if (!(ok = mbar_wait(&bars[B_FULL + st1], ((i + 1) / STAGES) & 1, wc, kErrWaitStageFull))) break;
-          if (!(ok = mbar_wait(&bars[B_PFREE], i & 1, wc, kErrWaitPFree))) break;
+          // dV += P^T dO: B = dO as [N = D] x [K = queries], MN-major; K-step = 16 rows = 2048 bytes
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + C::T_DV, sb + kk * 8, sdesc_sw128(sDO(st) + kk * 2048, C::Q_SLAB, 1024), IDESC_KV,
+                   j > 0 || kk > 0);
+          if (!(ok = mbar_wait(&bars[DS_READY], gs & 1, wc, kErrWaitDS))) break;
           tc_fence_after();
-          issue_S(st1);
-          mma_commit(&bars[B_S]);
-          issue_dP(st1);
-          mma_commit(&bars[B_DP]);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + C::T_DK, sb + BN / 2 + kk * 8, sdesc_sw128(sQ(st) + kk * 2048, C::Q_SLAB, 1024), IDESC_KV,
+                   j > 0 || kk > 0);
+          mma_commit(&bars[S_FREE0 + (gs & 1)]);  // P^T / dS^T of this buffer consumed
+          mma_commit(&bars[EMPTY0 + st]);         // every reader of this Q/dO stage issued
+          if (D == 128 && gs >= 1) {
+            if (!(ok = mbar_wait(&bars[DQ_EMPTY], (gs - 1) & 1, wc, kErrWaitDQEmpty))) break;
+            tc_fence_after();
+          }
+          // dQ over the 128 key rows (K-step = 16 key rows = 2048 bytes)
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            if constexpr (D == 128)  // dQ^T = K^T dS^T: A = K tile MN-major, B = dS^T MN-major
+              mma_ss(tmem + C::T_DQ, sdesc_sw128(sK + kk * 2048, C::KV_SLAB, 1024),
+                     sdesc_sw128(sDS + kk * 2048, C::KV_SLAB, 1024), IDESC_DQ, kk > 0);
+            else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
+              mma_ss(tmem + C::T_DQ, sdesc_sw128(sDS + kk * 2048, BM * 128, 1024),
+                     sdesc_sw128(sK + kk * 2048, C::KV_SLAB, 1024), IDESC_DQ, kk > 0);
+          }
+          mma_commit(&bars[DQ_FULL]);
+          mma_commit(&bars[DS_SFREE]);
+          if (j + 1 < n && !(ok = issue_dP(gs + 1))) break;
         }
+        if (!ok) break;
+        mma_commit(&bars[KV_FREE]);   // last readers of K and V issued
+        mma_commit(&bars[DKV_FULL]);  // dK, dV final once every MMA of the tile completed
       }
-      if (ok) mma_commit(&bars[B_DKV]);
       // every MMA issued by this thread completes before TMEM is released
-      mma_commit(&bars[B_DRAIN]);
-      mbar_drain(&bars[B_DRAIN], 0);
+      mma_commit(&bars[DRAIN]);
+      mbar_drain(&bars[DRAIN], 0);
     }
   } else if (warp >= 4) {
-    // ============================================================ softmax / dS
+    // ============================================================ softmax / dS, dK / dV landing
     const int wg = (warp - 4) >> 2, quad = warp & 3;
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
-    const int kpos = k0 + row;
-    const bool kvalid = kpos < len;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     constexpr int HALF = BN / 2;  // query columns of this warpgroup
     constexpr int NCH = HALF / 32;
@@ -327,108 +393,136 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int W = p.window;
     float pv[HALF];
     uint32_t dsw[HALF / 2];
+    uint32_t gs = 0;
     bool ok = true;
-    for (int i = 0; ok && i < n_steps; ++i) {
-      const int st = i % STAGES;
-      const int qc0 = (qlo + i % nq) * BN + wg * HALF;  // first query (sequence-local) of my columns
-      const float* lse = s_lse + st * BN + wg * HALF;
-      const float* dlt = s_delta + st * BN + wg * HALF;
-      if (!(ok = mbar_wait_warp(&bars[B_FULL + st], (i / STAGES) & 1, wc, kErrWaitStageFull))) break;
-      if (!(ok = mbar_wait_warp(&bars[B_S], i & 1, wc, kErrWaitS))) break;
-      tc_fence_after();
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+      const TileInfo ti = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+      if (!ti.valid) break;
+      const int n = p.G * ti.nq;
+      const int kpos = ti.k0 + row;
+      const bool kvalid = kpos < ti.len;
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
+        const uint32_t sb = tmem + lane_off + C::T_SB + (gs & 1u) * BN;
+        const int q0 = (ti.qlo + j % ti.nq) * BN;
+        const int qc0 = q0 + wg * HALF;  // first (sequence-local) query of my columns
+        // fully visible block: every key and query in range and inside the mask
+        const bool full_vis = ti.k0 + BM <= ti.len && q0 + BN <= ti.len && (!cm || q0 >= ti.k0 + BM - 1) &&
+                              (W <= 0 || q0 + BN - 1 < ti.k0 + W);
+        const float* lse = s_lse + st * BN + wg * HALF;
+        const float* dlt = s_delta + st * BN + wg * HALF;
+        if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
+        if (!(ok = mbar_wait_warp(&bars[S_FULL0 + (gs & 1)], (gs >> 1) & 1, wc, kErrWaitS))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::T_S + wg * HALF + ch * 32, r);
-        tmem_ld_wait();
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(sb + wg * HALF + ch * 32, r);
+          tmem_ld_wait();
+          if (full_vis) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int cc = ch * 32 + c, q = qc0 + cc;
-          bool vis = kvalid && q < len;
-          if (cm) vis = vis && kpos <= q;
-          if (W > 0) vis = vis && q < kpos + W;
-          pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[cc])) : 0.f;
+            for (int c = 0; c < 32; ++c)
+              pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[ch * 32 + c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int cc = ch * 32 + c, q = qc0 + cc;
+              bool vis = kvalid && q < ti.len;
+              if (cm) vis = vis && kpos <= q;
+              if (W > 0) vis = vis && q < kpos + W;
+              pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[cc])) : 0.f;
+            }
+          }
         }
-      }
-      // P^T overwrites S^T columns that the other warpgroup reads: all eight
-      // warps finish reading S^T first.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_SREAD]);
-      if (!(ok = mbar_wait_warp(&bars[B_SREAD], i & 1, wc, kErrWaitSRead))) break;
-      tc_fence_after();
+        // P^T overwrites S^T columns the other warpgroup reads: all eight
+        // warps finish reading S^T first.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[SREAD]);
+        if (!(ok = mbar_wait_warp(&bars[SREAD], gs & 1, wc, kErrWaitSRead))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        uint32_t w[16];
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
-        tmem_st16(tmem + lane_off + C::T_S + (wg * HALF + ch * 32) / 2, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_P]);
+          for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
+          tmem_st16(sb + (wg * HALF + ch * 32) / 2, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[P_READY]);
 
-      if (!(ok = mbar_wait_warp(&bars[B_DP], i & 1, wc, kErrWaitDP))) break;
-      tc_fence_after();
+        if (!(ok = mbar_wait_warp(&bars[DP_FULL], gs & 1, wc, kErrWaitDP))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + ch * 32, r);
-        tmem_ld_wait();
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + ch * 32, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int cc = ch * 32 + c;
-          const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[cc]);
-          const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[cc + 1]);
-          dsw[cc / 2] = pack2<BF16>(d0, d1);
+          for (int c = 0; c < 32; c += 2) {
+            const int cc = ch * 32 + c;
+            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[cc]);
+            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[cc + 1]);
+            dsw[cc / 2] = pack2<BF16>(d0, d1);
+          }
         }
+        if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DS_SFREE], (gs - 1) & 1, wc, kErrWaitDSFree))) break;
+        tc_fence_after();
+        // dS^T into the second half of this step's S^T buffer (its S^T is read)
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) tmem_st16(sb + BN / 2 + (wg * HALF + ch * 32) / 2, dsw + ch * 16);
+        if constexpr (D == 128) {
+          // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
+          // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``
+          uint8_t* base = sm + C::OFF_DS;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(base + sw128_offset(row, wg * 4 + c4)) =
+                make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+        } else {
+          // dS as the MN-major A operand: 64-query block wg, row = key
+          uint8_t* base = sm + C::OFF_DS + wg * (BM * 128);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(base + sw128_offset(row, c8)) =
+                make_uint4(dsw[c8 * 4], dsw[c8 * 4 + 1], dsw[c8 * 4 + 2], dsw[c8 * 4 + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[DS_READY]);
       }
-      if (i > 0 && !(ok = mbar_wait_warp(&bars[B_DSFREE], (i - 1) & 1, wc, kErrWaitDSFree))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) tmem_st16(tmem + lane_off + C::T_DS + (wg * HALF + ch * 32) / 2, dsw + ch * 16);
-      if constexpr (D == 128) {
-        // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
-        // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``
-        uint8_t* base = sm + C::OFF_DS;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4*>(base + sw128_offset(row, wg * 4 + c4)) =
-              make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
-      } else {
-        // dS as the MN-major A operand: 64-query block wg, row = key
-        uint8_t* base = sm + C::OFF_DS + wg * (BM * 128);
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(base + sw128_offset(row, c8)) =
-              make_uint4(dsw[c8 * 4], dsw[c8 * 4 + 1], dsw[c8 * 4 + 2], dsw[c8 * 4 + 3]);
-      }
-      fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_DS]);
-    }
-    // ---- dK / dV: warpgroup 0 lands dV, warpgroup 1 lands dK (times sm_scale)
-    if (ok && n_steps > 0) ok = mbar_wait_warp(&bars[B_DKV], 0, wc, kErrWaitDKV);
-    if (ok) {
+      if (!ok) break;
+      // ---- dK / dV of the tile: warpgroup 0 lands dV, warpgroup 1 lands dK (times sm_scale)
+      if (!(ok = mbar_wait_warp(&bars[DKV_FULL], tc & 1, wc, kErrWaitDKV))) break;
       tc_fence_after();
       const bool isK = wg == 1;
       const uint32_t col0 = isK ? C::T_DK : C::T_DV;
       const float mul = isK ? p.sm_scale : 1.f;
-      const int64_t pos = seq_start + kpos;
-      uint8_t* out = isK ? p.dk + 2 * (b * p.sdk_b + pos * p.sdk_s + g * p.sdk_h)
-                         : p.dv + 2 * (b * p.sdv_b + pos * p.sdv_s + g * p.sdv_h);
-#pragma unroll
+      const int64_t pos = ti.seq_start + kpos;
+      uint8_t* out = isK ? p.dk + 2 * (ti.b * p.sdk_b + pos * p.sdk_s + ti.g * p.sdk_h)
+                         : p.dv + 2 * (ti.b * p.sdv_b + pos * p.sdv_s + ti.g * p.sdv_h);
+#pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t r[32];
-        if (n_steps > 0) {
+        if (n > 0) {
           tmem_ld32(tmem + lane_off + col0 + ch * 32, r);
           tmem_ld_wait();
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
+        if (ch == D / 32 - 1) {  // the accumulators may be overwritten by the next tile from here on
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[DKV_FREE]);
         }
         if (kvalid) {
 #pragma unroll
@@ -447,40 +541,74 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     // ============================================================ dQ epilogue
     const int quad = warp;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    float* stg = reinterpret_cast<float*>(sm + C::OFF_STG);
+    const bool leader = warp == 0 && lane == 0;
+    bool issued = false;
+    uint32_t gs = 0;
     bool ok = true;
-    for (int i = 0; ok && i < n_steps; ++i) {
-      const int h = g * p.G + i / nq, q0 = (qlo + i % nq) * BN;
-      if (!(ok = mbar_wait_warp(&bars[B_DQFULL], i & 1, wc, kErrWaitDQFull))) break;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld32(tmem + lane_off + C::T_DQ, r);
-      tmem_ld32(tmem + lane_off + C::T_DQ + 32, r + 32);
-      tmem_ld_wait();
-      tc_fence_before();
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+      const TileInfo ti = ring[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_DQEMPTY]);
-      if constexpr (D == 128) {
-        // lane = head dim d, columns = the BN (= 64) queries of the block
-        const int d = quad * 32 + lane;
-        const int nvalid = imin(BN, len - q0);
-        float* base = p.dq_acc + ((static_cast<int64_t>(b) * p.S + seq_start + q0) * p.HQ + h) * D + d;
-        const int64_t qstride = static_cast<int64_t>(p.HQ) * D;
-#pragma unroll 8
-        for (int c = 0; c < 64; ++c)
-          if (c < nvalid) atomicAdd(base + c * qstride, __uint_as_float(r[c]));
-      } else {
-        // lane = query, columns = the 64 head dims
-        const int q = q0 + quad * 32 + lane;
-        if (q < len) {
-          float4* base = reinterpret_cast<float4*>(
-              p.dq_acc + ((static_cast<int64_t>(b) * p.S + seq_start + q) * p.HQ + h) * D);
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            atomicAdd(base + c, make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                            __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])));
+      if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+      if (!ti.valid) break;
+      const int n = p.G * ti.nq;
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
+        if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_off + C::T_DQ, r);
+        tmem_ld32(tmem + lane_off + C::T_DQ + 32, r + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[DQ_EMPTY]);
+        // the staging buffer is free once the previous bulk reduce has read it
+        if (leader) {
+          if (issued) bulk_wait_read_all();
+          mbar_arrive(&bars[STG_FREE]);
         }
+        if (!(ok = mbar_wait_warp(&bars[STG_FREE], gs & 1, wc, kErrWaitStage))) break;
+        if constexpr (D == 128) {
+          // lane = head dim d; staging [64 queries][128 d] f32, rows of 512 bytes
+          const int d = quad * 32 + lane;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) stg[c * 128 + d] = __uint_as_float(r[c]);
+        } else {
+          // lane = query; staging = two 128-byte-swizzled slabs [128 q][32 d]
+          const int q = quad * 32 + lane;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int slab = c >> 3, chunk = c & 7;
+            *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(stg) + slab * (128 * 128) + sw128_offset(q, chunk)) =
+                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
+                            __uint_as_float(r[4 * c + 3]));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[STG_FULL]);
+        bool lok = true;
+        if (leader) {
+          lok = mbar_wait(&bars[STG_FULL], gs & 1, wc, kErrWaitStage);
+          if (lok) {
+            const int c2 = ti.seq_start + q0;
+            if constexpr (D == 128) {
+              tma_reduce_add_4d(&maps.dq, stg, 0, h, c2, ti.b);
+            } else {
+              tma_reduce_add_4d(&maps.dq, stg, 0, h, c2, ti.b);
+              tma_reduce_add_4d(&maps.dq, reinterpret_cast<uint8_t*>(stg) + 128 * 128, 32, h, c2, ti.b);
+            }
+            bulk_commit_group();
+            issued = true;
+          }
+        }
+        if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
       }
     }
+    if (leader && issued) bulk_wait_all();
   }
 
   // ---------------------------------------------------------------- teardown

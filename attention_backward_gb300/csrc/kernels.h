@@ -49,10 +49,12 @@ struct DenseParams {
   uint8_t* dv;
   int64_t sdv_b, sdv_s, sdv_h;
   uint64_t timeout_ns;
+  int* tile_counter;  // zeroed by the preprocess; persistent CTAs draw tiles from it
 };
 
 struct DenseMaps {
   CUtensorMap q, k, v, dO;
+  CUtensorMap dq;  // f32 dQ accumulator [B,S,HQ,D] (bulk reduce-add target)
 };
 
 cudaError_t launch_preprocess(const PreprocessParams& p, bool bf16, int grid, cudaStream_t st);
