@@ -82,8 +82,9 @@ struct Cfg {
   static constexpr int T_DP = 2 * BN;      // dP^T f32 [128 x BN]
   static constexpr int T_DV = 3 * BN;      // dV f32 [128 x D]
   static constexpr int T_DK = 3 * BN + D;  // dK f32 [128 x D]
-  // dQ^T [128 d x 64 q] in its own columns (D = 128); dQ [128 q x 64 d] over dP^T (D = 64)
-  static constexpr int T_DQ = D == 128 ? 3 * BN + 2 * D : T_DP;
+  // dQ^T [128 d x 64 q] in its own columns (D = 128); for D = 64, dQ [128 q x 64 d]
+  // goes into the first 64 columns of its step's S^T buffer once dK has read that buffer
+  static constexpr int T_DQ = 3 * BN + 2 * D;
   static_assert(3 * BN + 2 * D + (D == 128 ? 64 : 0) <= 512, "TMEM budget");
   static constexpr int THREADS = 14 * 32;
 };
@@ -98,8 +99,8 @@ enum Bar : int {
   S_FULL0 = 12,     // 2 buffers
   S_FREE0 = 14,     // 2 buffers
   SREAD = 16,
-  P_READY,
-  DP_FULL,
+  P_READY0,  // 2 buffers
+  DP_FULL = 19,
   DS_READY,
   DS_SFREE,
   DQ_FULL,
@@ -109,8 +110,11 @@ enum Bar : int {
   DKV_FULL,
   DKV_FREE,
   DRAIN,
+  DP_FREE,
+  DK_DONE,
   NUM_BARS
 };
+static_assert(NUM_BARS <= 32, "barrier storage");
 
 struct TileInfo {
   int b, g, seq_start, len, k0, qlo, nq, valid;
@@ -185,7 +189,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       mbar_init(&bars[S_FREE0 + i], 1);
     }
     mbar_init(&bars[SREAD], 8);
-    mbar_init(&bars[P_READY], 8);
+    mbar_init(&bars[P_READY0], 8);
+    mbar_init(&bars[P_READY0 + 1], 8);
     mbar_init(&bars[DP_FULL], 1);
     mbar_init(&bars[DS_READY], 8);
     mbar_init(&bars[DS_SFREE], 1);
@@ -196,6 +201,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[DKV_FULL], 1);
     mbar_init(&bars[DKV_FREE], 8);
     mbar_init(&bars[DRAIN], 1);
+    mbar_init(&bars[DP_FREE], 8);
+    mbar_init(&bars[DK_DONE], 1);
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -283,105 +290,145 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     }
   } else if (warp == 13) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, BN, false, false);
-      constexpr uint32_t IDESC_KV = idesc_f16(BF16, 128, D, false, true);
-      constexpr uint32_t IDESC_DQ = idesc_f16(BF16, 128, 64, true, true);
-      const uint32_t sK = smem_u32(sm + C::OFF_K), sV = smem_u32(sm + C::OFF_V), sDS = smem_u32(sm + C::OFF_DS);
-      auto sQ = [&](int st) { return smem_u32(sm + C::OFF_Q + st * C::Q_TILE); };
-      auto sDO = [&](int st) { return smem_u32(sm + C::OFF_DO + st * C::Q_TILE); };
-      auto tSB = [&](uint32_t s) { return tmem + C::T_SB + (s & 1u) * BN; };
-
-      // S^T of global step s into its buffer (waits for its stage and for the
-      // buffer's previous P^T/dS^T readers).  K-major operands: K-step kk of
-      // 16 elements = slab kk/4, byte offset 32*(kk%4).
-      auto issue_S = [&](uint32_t s) -> bool {
-        if (!mbar_wait(&bars[FULL0 + s % ST], (s / ST) & 1, wc, kErrWaitStageFull)) return false;
-        if (s >= 2 && !mbar_wait(&bars[S_FREE0 + (s & 1)], ((s - 2) >> 1) & 1, wc, kErrWaitSFree)) return false;
-        tc_fence_after();
-        const uint32_t q = sQ(s % ST);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk / 4) * C::KV_SLAB + (kk % 4) * 32, qo = (kk / 4) * C::Q_SLAB + (kk % 4) * 32;
-          mma_ss(tSB(s), sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(q + qo, 16, 1024), IDESC_S, kk > 0);
-        }
-        mma_commit(&bars[S_FULL0 + (s & 1)]);
-        return true;
-      };
-      // dP^T of step s (its stage is known full: issue_S(s) waited for it).
-      auto issue_dP = [&](uint32_t s) -> bool {
-        if (D == 64 && s >= 1) {  // dQ of step s-1 lives in the dP^T columns until the epilogue read it
-          if (!mbar_wait(&bars[DQ_EMPTY], (s - 1) & 1, wc, kErrWaitDQEmpty)) return false;
-          tc_fence_after();
-        }
-        const uint32_t o = sDO(s % ST);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk / 4) * C::KV_SLAB + (kk % 4) * 32, qo = (kk / 4) * C::Q_SLAB + (kk % 4) * 32;
-          mma_ss(tmem + C::T_DP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(o + qo, 16, 1024), IDESC_S, kk > 0);
-        }
-        mma_commit(&bars[DP_FULL]);
-        return true;
-      };
-
-      uint32_t gs = 0;
-      bool ok = true;
-      for (int tc = 0; ok; ++tc) {
-        const int slot = tc & 1;
-        if (!(ok = mbar_wait(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
-        const TileInfo ti = ring[slot];
-        mbar_arrive(&bars[TILE_EMPTY0 + slot]);
-        if (!ti.valid) break;
-        const int n = p.G * ti.nq;
-        if (!(ok = mbar_wait(&bars[KV_FULL], tc & 1, wc, kErrWaitKV))) break;
-        tc_fence_after();
-        if (n > 0 && (!(ok = issue_S(gs)) || !(ok = issue_dP(gs)))) break;
-        for (int j = 0; j < n; ++j, ++gs) {
-          const int st = gs % ST;
-          const uint32_t sb = tSB(gs);
-          if (j + 1 < n && !(ok = issue_S(gs + 1))) break;
-          if (!(ok = mbar_wait(&bars[P_READY], gs & 1, wc, kErrWaitP))) break;
-          if (j == 0 && tc >= 1 && !(ok = mbar_wait(&bars[DKV_FREE], (tc - 1) & 1, wc, kErrWaitDKVFree))) break;
-          tc_fence_after();
-          // dV += P^T dO: B = dO as [N = D] x [K = queries], MN-major; K-step = 16 rows = 2048 bytes
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + C::T_DV, sb + kk * 8, sdesc_sw128(sDO(st) + kk * 2048, C::Q_SLAB, 1024), IDESC_KV,
-                   j > 0 || kk > 0);
-          if (!(ok = mbar_wait(&bars[DS_READY], gs & 1, wc, kErrWaitDS))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + C::T_DK, sb + BN / 2 + kk * 8, sdesc_sw128(sQ(st) + kk * 2048, C::Q_SLAB, 1024), IDESC_KV,
-                   j > 0 || kk > 0);
-          mma_commit(&bars[S_FREE0 + (gs & 1)]);  // P^T / dS^T of this buffer consumed
-          mma_commit(&bars[EMPTY0 + st]);         // every reader of this Q/dO stage issued
-          if (D == 128 && gs >= 1) {
-            if (!(ok = mbar_wait(&bars[DQ_EMPTY], (gs - 1) & 1, wc, kErrWaitDQEmpty))) break;
-            tc_fence_after();
+    // The whole warp runs this role with warp-uniform values; one elected lane
+    // issues each tcgen05 instruction.
+    constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, BN, false, false);
+    constexpr uint32_t IDESC_KV = idesc_f16(BF16, 128, D, false, true);
+    constexpr uint32_t IDESC_DQ = idesc_f16(BF16, 128, 64, true, true);
+    const uint32_t sbase = smem_u32(sm);
+    // descriptors at the start of each operand; K-major K-steps add 32 bytes
+    // inside a 128-byte row (slab kk/4), MN-major K-steps add 16 rows = 2048 bytes
+    const uint64_t dK_kmaj = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t dV_kmaj = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+    const uint64_t dQ_kmaj = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+    const uint64_t dO_kmaj = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+    const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::Q_SLAB, 1024);
+    const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::Q_SLAB, 1024);
+    const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::KV_SLAB, 1024);
+    const uint64_t dDS_mn = sdesc_sw128(sbase + C::OFF_DS, BM * 128, 1024);
+    int64_t last_dq = -1;  // global step of the most recently issued dQ
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+      const TileInfo ti = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+      if (!ti.valid) break;
+      const int n = p.G * ti.nq;
+      if (!(ok = mbar_wait_warp(&bars[KV_FULL], tc & 1, wc, kErrWaitKV))) break;
+      tc_fence_after();
+      for (int j = -1; j < n; ++j) {
+        // j = -1: the tile's first S^T and dP^T; then per step j: the next
+        // step's S^T, this step's dV, the next step's dP^T, this step's dK, dQ.
+        const uint32_t cur = gs;               // step j (when j >= 0)
+        const uint32_t nxt = j < 0 ? gs : gs + 1;  // step whose S^T / dP^T is issued now
+        if (j + 1 < n) {
+          // ---- S^T of step nxt into buffer nxt & 1
+          const int st = nxt % ST;
+          if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (nxt / ST) & 1, wc, kErrWaitStageFull))) break;
+          if (nxt >= 2) {
+            // the buffer's previous readers: dV/dK of step nxt-2 (D = 128), or the
+            // epilogue's readout of the dQ that overwrote it (D = 64; readouts are
+            // in step order, so the latest issued dQ is waited for)
+            const bool ok2 = D == 128
+                                 ? mbar_wait_warp(&bars[S_FREE0 + (nxt & 1)], ((nxt - 2) >> 1) & 1, wc, kErrWaitSFree)
+                                 : mbar_wait_warp(&bars[DQ_EMPTY], static_cast<uint32_t>(last_dq) & 1, wc,
+                                                  kErrWaitDQEmpty);
+            if (!(ok = ok2)) break;
           }
-          // dQ over the 128 key rows (K-step = 16 key rows = 2048 bytes)
+          tc_fence_after();
+          const uint32_t dS_acc = tmem + C::T_SB + (nxt & 1) * BN;
+          const uint64_t qo = sdesc_step(st * C::Q_TILE);
 #pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            if constexpr (D == 128)  // dQ^T = K^T dS^T: A = K tile MN-major, B = dS^T MN-major
-              mma_ss(tmem + C::T_DQ, sdesc_sw128(sK + kk * 2048, C::KV_SLAB, 1024),
-                     sdesc_sw128(sDS + kk * 2048, C::KV_SLAB, 1024), IDESC_DQ, kk > 0);
-            else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
-              mma_ss(tmem + C::T_DQ, sdesc_sw128(sDS + kk * 2048, BM * 128, 1024),
-                     sdesc_sw128(sK + kk * 2048, C::KV_SLAB, 1024), IDESC_DQ, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ko = sdesc_step((kk / 4) * C::KV_SLAB + (kk % 4) * 32);
+            const uint64_t qk = sdesc_step((kk / 4) * C::Q_SLAB + (kk % 4) * 32);
+            mma_ss_w(dS_acc, dK_kmaj + ko, dQ_kmaj + qo + qk, IDESC_S, kk > 0);
           }
-          mma_commit(&bars[DQ_FULL]);
-          mma_commit(&bars[DS_SFREE]);
-          if (j + 1 < n && !(ok = issue_dP(gs + 1))) break;
+          mma_commit_w(&bars[S_FULL0 + (nxt & 1)]);
+          if (j < 0) {
+            // ---- dP^T of the tile's first step
+            if (nxt >= 1) {
+              if (!(ok = mbar_wait_warp(&bars[DP_FREE], (nxt - 1) & 1, wc, kErrWaitDP))) break;
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t ko = sdesc_step((kk / 4) * C::KV_SLAB + (kk % 4) * 32);
+              const uint64_t qk = sdesc_step((kk / 4) * C::Q_SLAB + (kk % 4) * 32);
+              mma_ss_w(tmem + C::T_DP, dV_kmaj + ko, dO_kmaj + qo + qk, IDESC_S, kk > 0);
+            }
+            mma_commit_w(&bars[DP_FULL]);
+          }
         }
-        if (!ok) break;
-        mma_commit(&bars[KV_FREE]);   // last readers of K and V issued
-        mma_commit(&bars[DKV_FULL]);  // dK, dV final once every MMA of the tile completed
+        if (j < 0) continue;
+        const int st = cur % ST;
+        const uint64_t qo = sdesc_step(st * C::Q_TILE);
+        const uint32_t sb = tmem + C::T_SB + (cur & 1) * BN;
+        // ---- dV += P^T dO (B = dO as [N = D] x [K = queries], MN-major)
+        if (!(ok = mbar_wait_warp(&bars[P_READY0 + (cur & 1)], (cur >> 1) & 1, wc, kErrWaitP))) break;
+        if (j == 0 && tc >= 1 && !(ok = mbar_wait_warp(&bars[DKV_FREE], (tc - 1) & 1, wc, kErrWaitDKVFree))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_w(tmem + C::T_DV, sb + kk * 8, dO_mn + qo + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
+        // ---- dP^T of the next step, as soon as this step's dP^T has been loaded
+        if (j + 1 < n) {
+          if (!(ok = mbar_wait_warp(&bars[DP_FREE], cur & 1, wc, kErrWaitDP))) break;
+          tc_fence_after();
+          const uint64_t qn = sdesc_step(((cur + 1) % ST) * C::Q_TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ko = sdesc_step((kk / 4) * C::KV_SLAB + (kk % 4) * 32);
+            const uint64_t qk = sdesc_step((kk / 4) * C::Q_SLAB + (kk % 4) * 32);
+            mma_ss_w(tmem + C::T_DP, dV_kmaj + ko, dO_kmaj + qn + qk, IDESC_S, kk > 0);
+          }
+          mma_commit_w(&bars[DP_FULL]);
+        }
+        // ---- dK += dS^T Q (B = Q as [N = D] x [K = queries], MN-major)
+        if (!(ok = mbar_wait_warp(&bars[DS_READY], cur & 1, wc, kErrWaitDS))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_w(tmem + C::T_DK, sb + BN / 2 + kk * 8, dQ_mn + qo + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
+        mma_commit_w(&bars[EMPTY0 + st]);  // every reader of this Q/dO stage issued
+        uint32_t dq_cols;
+        if constexpr (D == 128) {
+          mma_commit_w(&bars[S_FREE0 + (cur & 1)]);  // P^T / dS^T of this buffer consumed
+          dq_cols = tmem + C::T_DQ;
+        } else {
+          // dQ overwrites this step's S^T buffer: dV and dK must have read it
+          mma_commit_w(&bars[DK_DONE]);
+          if (!(ok = mbar_wait_warp(&bars[DK_DONE], cur & 1, wc, kErrWaitSFree))) break;
+          dq_cols = sb;
+        }
+        // one dQ in flight: the epilogue has read the previous one
+        if (cur >= 1 && !(ok = mbar_wait_warp(&bars[DQ_EMPTY], (cur - 1) & 1, wc, kErrWaitDQEmpty))) break;
+        tc_fence_after();
+        // ---- dQ over the 128 key rows (K-step = 16 key rows = 2048 bytes)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          if constexpr (D == 128)  // dQ^T = K^T dS^T: A = K tile MN-major, B = dS^T MN-major
+            mma_ss_w(dq_cols, dK_mn + sdesc_step(kk * 2048), dDS_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
+          else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
+            mma_ss_w(dq_cols, dDS_mn + sdesc_step(kk * 2048), dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
+        }
+        mma_commit_w(&bars[DQ_FULL]);
+        mma_commit_w(&bars[DS_SFREE]);
+        last_dq = cur;
+        ++gs;
       }
-      // every MMA issued by this thread completes before TMEM is released
-      mma_commit(&bars[DRAIN]);
-      mbar_drain(&bars[DRAIN], 0);
+      if (!ok) break;
+      if (n == 0 && tc >= 1 && !(ok = mbar_wait_warp(&bars[DKV_FREE], (tc - 1) & 1, wc, kErrWaitDKVFree))) break;
+      mma_commit_w(&bars[KV_FREE]);   // last readers of K and V issued
+      mma_commit_w(&bars[DKV_FULL]);  // dK, dV final once every MMA of the tile completed
     }
+    // every MMA issued by this warp completes before TMEM is released
+    mma_commit_w(&bars[DRAIN]);
+    if (lane == 0) mbar_drain(&bars[DRAIN], 0);
+    __syncwarp();
   } else if (warp >= 4) {
     // ============================================================ softmax / dS, dK / dV landing
     const int wg = (warp - 4) >> 2, quad = warp & 3;
@@ -455,7 +502,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[P_READY]);
+        if (lane == 0) mbar_arrive(&bars[P_READY0 + (gs & 1)]);
 
         if (!(ok = mbar_wait_warp(&bars[DP_FULL], gs & 1, wc, kErrWaitDP))) break;
         tc_fence_after();
@@ -464,6 +511,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + ch * 32, r);
           tmem_ld_wait();
+          if (ch == NCH - 1) {  // dP^T fully loaded: the next step's dP^T may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[DP_FREE]);
+          }
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const int cc = ch * 32 + c;
@@ -559,8 +611,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
         uint32_t r[64];
-        tmem_ld32(tmem + lane_off + C::T_DQ, r);
-        tmem_ld32(tmem + lane_off + C::T_DQ + 32, r + 32);
+        const uint32_t dq_cols = tmem + lane_off + (D == 128 ? C::T_DQ : C::T_SB + (gs & 1u) * BN);
+        tmem_ld32(dq_cols, r);
+        tmem_ld32(dq_cols + 32, r + 32);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
