@@ -55,12 +55,14 @@ struct Cfg {
   static constexpr int BM = kDenseBM;
   static constexpr int BN = dense_bn(D);
   static constexpr int STAGES = 3;
+  static constexpr int PREFETCH = 8;  // L2 prefetch distance of Q/dO/LSE/delta, in steps
   static constexpr int NSLAB = D / 64;  // 64-column (128-byte) slabs per row
   static constexpr int KV_SLAB = BM * 128;
   static constexpr int KV_TILE = KV_SLAB * NSLAB;
   static constexpr int Q_SLAB = BN * 128;
   static constexpr int Q_TILE = Q_SLAB * NSLAB;
   static constexpr int DS_BYTES = BM * BN * 2;
+  static constexpr int NDS = D == 128 ? 2 : 1;  // dS tiles in shared memory (double-buffered when they fit)
   static constexpr int STG_BYTES = BN * D * 4;  // f32 dQ staging of one step
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
@@ -68,7 +70,7 @@ struct Cfg {
   static constexpr int OFF_Q = OFF_V + KV_TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_TILE;
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
-  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
+  static constexpr int OFF_STG = OFF_DS + NDS * DS_BYTES;
   static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
   static constexpr int OFF_DELTA = OFF_LSE + STAGES * BN * 4;
   static constexpr int OFF_RING = OFF_DELTA + STAGES * BN * 4;
@@ -102,8 +104,8 @@ enum Bar : int {
   P_READY0,  // 2 buffers
   DP_FULL = 19,
   DS_READY,
-  DS_SFREE,
-  DQ_FULL,
+  DS_SFREE0,  // NDS buffers (up to 2)
+  DQ_FULL = DS_SFREE0 + 2,
   DQ_EMPTY,
   STG_FREE,
   STG_FULL,
@@ -162,7 +164,7 @@ __device__ TileInfo decode_tile(int t, const DenseParams& p) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
   using C = Cfg<D>;
-  constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES;
+  constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES, kPrefetch = C::PREFETCH;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
@@ -193,7 +195,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[P_READY0 + 1], 8);
     mbar_init(&bars[DP_FULL], 1);
     mbar_init(&bars[DS_READY], 8);
-    mbar_init(&bars[DS_SFREE], 1);
+    mbar_init(&bars[DS_SFREE0], 1);
+    mbar_init(&bars[DS_SFREE0 + 1], 1);
     mbar_init(&bars[DQ_FULL], 1);
     mbar_init(&bars[DQ_EMPTY], 4);
     mbar_init(&bars[STG_FREE], 1);
@@ -248,6 +251,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       }
       kv_pend = tc & 1;
       const int n = p.G * ti.nq;
+      // LSE2 / delta of a step are loaded into registers one step ahead, so
+      // their global-load latency hides behind the next stage wait.
+      constexpr int PER_LANE = BN / 32;
+      float nl[PER_LANE], nd[PER_LANE];
+      auto load_rows = [&](int jj) {
+        const int hh = ti.g * p.G + jj / ti.nq, qq = (ti.qlo + jj % ti.nq) * BN;
+        const int64_t rb = (static_cast<int64_t>(ti.b) * p.HQ + hh) * p.S + ti.seq_start;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+          const int q = qq + lane + 32 * i;
+          nl[i] = q < ti.len ? p.lse2[rb + q] : 0.f;
+          nd[i] = q < ti.len ? p.delta[rb + q] : 0.f;
+        }
+      };
+      if (n > 0) load_rows(0);
       for (int j = 0; j < n; ++j, ++gs) {
         const int st = gs % ST;
         const uint32_t r = gs / ST;
@@ -255,18 +273,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             !(ok = mbar_wait_warp(&bars[EMPTY0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
           break;
         const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
-        const int64_t rowbase = (static_cast<int64_t>(ti.b) * p.HQ + h) * p.S + ti.seq_start;
-        for (int c = lane; c < BN; c += 32) {
-          const int q = q0 + c;
-          float l = 0.f, d = 0.f;
-          if (q < ti.len) {
-            l = p.lse2[rowbase + q];
-            d = p.delta[rowbase + q];
-          }
-          s_lse[st * BN + c] = l;
-          s_delta[st * BN + c] = d;
-        }
-        __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars[FULL0 + st], 2 * C::Q_TILE);
 #pragma unroll
@@ -276,8 +282,31 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             tma_load_4d(sm + C::OFF_DO + st * C::Q_TILE + s * C::Q_SLAB, &maps.dO, &bars[FULL0 + st], s * 64, h,
                         ti.seq_start + q0, ti.b);
           }
-          mbar_arrive(&bars[FULL0 + st]);
         }
+        // warm L2 with the operands of a step kPrefetch steps ahead
+        if (j + kPrefetch < n) {
+          const int hf = ti.g * p.G + (j + kPrefetch) / ti.nq, qf = (ti.qlo + (j + kPrefetch) % ti.nq) * BN;
+          if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < C::NSLAB; ++s) {
+              tma_prefetch_l2_4d(&maps.q, s * 64, hf, ti.seq_start + qf, ti.b);
+              tma_prefetch_l2_4d(&maps.dO, s * 64, hf, ti.seq_start + qf, ti.b);
+            }
+          }
+          const int64_t rf = (static_cast<int64_t>(ti.b) * p.HQ + hf) * p.S + ti.seq_start + qf;
+          if (lane < BN / 32 && qf + lane * 32 < ti.len) {
+            prefetch_l2(p.lse2 + rf + lane * 32);
+            prefetch_l2(p.delta + rf + lane * 32);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+          s_lse[st * BN + lane + 32 * i] = nl[i];
+          s_delta[st * BN + lane + 32 * i] = nd[i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[FULL0 + st]);
+        if (j + 1 < n) load_rows(j + 1);
         pend_full[st] = r & 1;
       }
     }
@@ -411,12 +440,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk) {
           if constexpr (D == 128)  // dQ^T = K^T dS^T: A = K tile MN-major, B = dS^T MN-major
-            mma_ss_w(dq_cols, dK_mn + sdesc_step(kk * 2048), dDS_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
+            mma_ss_w(dq_cols, dK_mn + sdesc_step(kk * 2048),
+                     dDS_mn + sdesc_step((cur % C::NDS) * C::DS_BYTES + kk * 2048), IDESC_DQ, kk > 0);
           else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
             mma_ss_w(dq_cols, dDS_mn + sdesc_step(kk * 2048), dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
         }
         mma_commit_w(&bars[DQ_FULL]);
-        mma_commit_w(&bars[DS_SFREE]);
+        mma_commit_w(&bars[DS_SFREE0 + cur % C::NDS]);
         last_dq = cur;
         ++gs;
       }
@@ -460,8 +490,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         // fully visible block: every key and query in range and inside the mask
         const bool full_vis = ti.k0 + BM <= ti.len && q0 + BN <= ti.len && (!cm || q0 >= ti.k0 + BM - 1) &&
                               (W <= 0 || q0 + BN - 1 < ti.k0 + W);
-        const float* lse = s_lse + st * BN + wg * HALF;
-        const float* dlt = s_delta + st * BN + wg * HALF;
+        const float4* lse4 = reinterpret_cast<const float4*>(s_lse + st * BN + wg * HALF);
+        const float4* dlt4 = reinterpret_cast<const float4*>(s_delta + st * BN + wg * HALF);
         if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
         if (!(ok = mbar_wait_warp(&bars[S_FULL0 + (gs & 1)], (gs >> 1) & 1, wc, kErrWaitS))) break;
         tc_fence_after();
@@ -469,11 +499,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
           tmem_ld32(sb + wg * HALF + ch * 32, r);
+          float lse[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 t = lse4[ch * 8 + c4];
+            lse[4 * c4] = t.x, lse[4 * c4 + 1] = t.y, lse[4 * c4 + 2] = t.z, lse[4 * c4 + 3] = t.w;
+          }
           tmem_ld_wait();
           if (full_vis) {
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-              pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[ch * 32 + c]));
+              pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c]));
           } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -481,7 +517,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
               bool vis = kvalid && q < ti.len;
               if (cm) vis = vis && kpos <= q;
               if (W > 0) vis = vis && q < kpos + W;
-              pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[cc])) : 0.f;
+              pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c])) : 0.f;
             }
           }
         }
@@ -510,6 +546,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + ch * 32, r);
+          float dlt[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 t = dlt4[ch * 8 + c4];
+            dlt[4 * c4] = t.x, dlt[4 * c4 + 1] = t.y, dlt[4 * c4 + 2] = t.z, dlt[4 * c4 + 3] = t.w;
+          }
           tmem_ld_wait();
           if (ch == NCH - 1) {  // dP^T fully loaded: the next step's dP^T may overwrite it
             tc_fence_before();
@@ -519,12 +561,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const int cc = ch * 32 + c;
-            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[cc]);
-            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[cc + 1]);
+            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[c]);
+            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[c + 1]);
             dsw[cc / 2] = pack2<BF16>(d0, d1);
           }
         }
-        if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DS_SFREE], (gs - 1) & 1, wc, kErrWaitDSFree))) break;
+        // the dS tile this step writes was last read by the dQ of step gs - NDS
+        if (gs >= static_cast<uint32_t>(C::NDS) &&
+            !(ok = mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree)))
+          break;
         tc_fence_after();
         // dS^T into the second half of this step's S^T buffer (its S^T is read)
 #pragma unroll
@@ -532,7 +577,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         if constexpr (D == 128) {
           // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
           // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``
-          uint8_t* base = sm + C::OFF_DS;
+          uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES;
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
             *reinterpret_cast<uint4*>(base + sw128_offset(row, wg * 4 + c4)) =

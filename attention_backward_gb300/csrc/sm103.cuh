@@ -66,10 +66,8 @@ __device__ __forceinline__ void raise_error(const WaitCtx& c, int code) {
   atomicCAS(c.err, 0, code);
 }
 
-// Waits for phase ``parity`` of ``bar`` to complete. Returns false (and leaves
-// the abort flag raised) if the CTA is aborting or the wait timed out.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
-  if (mbar_try(bar, parity)) return true;
+// Slow path of mbar_wait: bounded polling with abort and error checks.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
@@ -85,6 +83,15 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Wai
       return false;
     }
   }
+}
+
+// Waits for phase ``parity`` of ``bar`` to complete. Returns false (and leaves
+// the abort flag raised) if the CTA is aborting or the wait timed out.  The
+// first probe is inline: a wait whose phase has already completed costs one
+// try_wait, not a call.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, code);
 }
 
 // Warp-uniform wait: every lane polls, and the warp proceeds only if all
@@ -129,6 +136,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "[%6];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+// Prefetch of a tiled box into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* m, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
 // Plain (untensored) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
