@@ -51,6 +51,9 @@ _SIGS = {
     "attn_bwd_query_block_range": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                           ctypes.POINTER(c_i32)]),
     "attn_bwd_selftest_timeout": (c_i32, [c_vp, c_sz, c_i32, c_vp]),
+    "attn_bwd_gqa_noalloc": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides,
+                                     c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32,
+                                     ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -262,3 +265,25 @@ def sparse_backward(q, kv, o, do, lse, idx, sm_scale: Optional[float] = None, dv
     attn_bwd_sparse(q, kv, do, idx, workspace, sm_scale, dv_dim, stream)
     sparse_land(dq, dkv, workspace, stream)
     return dq, dkv
+
+
+def backward_noalloc(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1,
+                     cu_seqlens=None, stream=None):
+    """dQ, dK, dV through attn_bwd_gqa_noalloc: the library's own device
+    workspace instead of a caller-provided one (for callers that cannot
+    allocate device memory).  Calls on one device must not overlap on the GPU.
+    The output tensors here are allocated by torch for convenience; a caller
+    without an allocator passes its own buffers to the C entry point."""
+    _dev(q, k, v, o, do, lse)
+    B, S, HQ, D = q.shape
+    HKV = k.shape[2]
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    m = _mask(causal, window, cu_seqlens)
+    _status(library().attn_bwd_gqa_noalloc(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
+                                           o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(),
+                                           _lse_strides(lse), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
+                                           ctypes.byref(m), dq.data_ptr(), _bshd(dq), dk.data_ptr(), _bshd(dk),
+                                           dv.data_ptr(), _bshd(dv), _stream(stream)), "attn_bwd_gqa_noalloc")
+    return dq, dk, dv

@@ -185,6 +185,39 @@ ATTN_BWD_API void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_
  * works).  Needs a workspace of at least 256 bytes. */
 ATTN_BWD_API attn_status_t attn_bwd_selftest_timeout(void* workspace, size_t workspace_bytes, int32_t timeout_us, void* stream);
 
+/* Size of the library-held workspace of attn_bwd_gqa_noalloc (32 MiB). */
+#define ATTN_BWD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* The whole dense backward (attn_bwd_preprocess, attn_bwd_gqa and
+ * attn_bwd_dq_land on ``stream``) for callers that cannot allocate device
+ * memory: plugins running inside a framework that owns all device memory
+ * through its own pool, and latency-critical loops that cannot afford the
+ * device-wide synchronisation of cudaMalloc/cudaFree.  This entry point is a
+ * convenience of this library; the pages it follows have no counterpart.
+ *
+ * Instead of a workspace argument it uses one device array of
+ * ATTN_BWD_NOALLOC_SCRATCH_BYTES that the library holds, on every GPU that
+ * loads it, until the process exits; it allocates nothing.  Problems whose
+ * attn_bwd_workspace_size(B, S, HQ, D, 0) exceeds that size are rejected with
+ * ATTN_ERR_WORKSPACE before anything is queued.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls on a
+ * device share the array: calls whose work overlaps on the GPU (different
+ * streams, or several host threads) race and corrupt each other's results, so
+ * serialise them.  The preprocess clears what must start at zero, so earlier
+ * calls' leftovers do not matter.  attn_bwd_check_error cannot inspect this
+ * array; a kernel fault is still reported by CUDA at the next synchronisation.
+ *   q, o, dO, dq : [B,S,HQ,D];  k, v, dk, dv : [B,S,HKV,D] (16-bit);
+ *   lse : f32 [B,HQ,S] (natural log) with strides slse (b, s, h);
+ *   the other arguments as for attn_bwd_preprocess / attn_bwd_gqa. */
+ATTN_BWD_API attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
+                                                const void* v, attn_strides_t sv, const void* o, attn_strides_t so,
+                                                const void* dO, attn_strides_t sdo, const float* lse,
+                                                attn_strides_t slse, int64_t B, int64_t S, int64_t HQ, int64_t HKV,
+                                                int64_t D, attn_dtype_t dtype, float sm_scale,
+                                                const attn_mask_t* mask, void* dq, attn_strides_t sdq, void* dk,
+                                                attn_strides_t sdk, void* dv, attn_strides_t sdv, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
