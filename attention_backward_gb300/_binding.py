@@ -43,9 +43,9 @@ _SIGS = {
                          c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, c_sz, c_vp]),
     "attn_bwd_dq_land": (c_i32, [c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, c_sz, c_vp]),
     "attn_bwd_sparse": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64,
-                                c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, c_sz, c_vp]),
-    "attn_bwd_sparse_land": (c_i32, [c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32,
-                                     c_vp, c_sz, c_vp]),
+                                c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd_sparse_land": (c_i32, [c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_vp, c_sz,
+                                     c_vp]),
     "attn_bwd_check_error": (c_i32, [c_vp, c_vp, ctypes.POINTER(c_i32)]),
     "attn_bwd_status_string": (ctypes.c_char_p, [c_i32]),
     "attn_bwd_query_block_range": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
@@ -177,9 +177,9 @@ def dq_land(dq, workspace, sm_scale: float, stream=None) -> None:
             "attn_bwd_dq_land")
 
 
-def attn_bwd_sparse(q, kv, do, idx, workspace, sm_scale: float, dv_dim: int, stream=None) -> None:
-    """Launch 2 of the top-k sparse path (see attn_bwd_sparse)."""
-    _dev(q, kv, do, idx, workspace)
+def attn_bwd_sparse(q, kv, do, idx, dq, workspace, sm_scale: float, dv_dim: int, stream=None) -> None:
+    """Launch 2 of the top-k sparse path: writes dQ, accumulates dKV (see attn_bwd_sparse)."""
+    _dev(q, kv, do, idx, dq, workspace)
     B, S, H, DQK = q.shape
     SKV, HKV = kv.shape[1], kv.shape[2]
     if idx.dtype != torch.int32 or idx.dim() != 4 or idx.stride(3) != 1:
@@ -187,17 +187,17 @@ def attn_bwd_sparse(q, kv, do, idx, workspace, sm_scale: float, dv_dim: int, str
     topk = idx.shape[3]
     _status(library().attn_bwd_sparse(q.data_ptr(), _bshd(q), kv.data_ptr(), _bshd(kv), do.data_ptr(), _bshd(do),
                                       idx.data_ptr(), Strides(idx.stride(0), idx.stride(1), idx.stride(2)), B, S,
-                                      SKV, H, HKV, DQK, dv_dim, topk, _dt(q), float(sm_scale),
-                                      workspace.data_ptr(), workspace.numel(), _stream(stream)), "attn_bwd_sparse")
+                                      SKV, H, HKV, DQK, dv_dim, topk, _dt(q), float(sm_scale), dq.data_ptr(),
+                                      _bshd(dq), workspace.data_ptr(), workspace.numel(), _stream(stream)),
+            "attn_bwd_sparse")
 
 
-def sparse_land(dq, dkv, workspace, stream=None) -> None:
-    """Launch 3 of the sparse path: dQ and dKV cast from their accumulators."""
-    _dev(dq, dkv, workspace)
-    B, S, H, DQK = dq.shape
-    SKV, HKV = dkv.shape[1], dkv.shape[2]
-    _status(library().attn_bwd_sparse_land(dq.data_ptr(), _bshd(dq), dkv.data_ptr(), _bshd(dkv), B, S, SKV, H, HKV,
-                                           DQK, _dt(dq), workspace.data_ptr(), workspace.numel(), _stream(stream)),
+def sparse_land(dkv, workspace, B: int, S: int, H: int, stream=None) -> None:
+    """Launch 3 of the sparse path: dKV cast from its accumulator."""
+    _dev(dkv, workspace)
+    _, SKV, HKV, DQK = dkv.shape
+    _status(library().attn_bwd_sparse_land(dkv.data_ptr(), _bshd(dkv), B, S, SKV, H, HKV, DQK, _dt(dkv),
+                                           workspace.data_ptr(), workspace.numel(), _stream(stream)),
             "attn_bwd_sparse_land")
 
 
@@ -249,7 +249,8 @@ def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool
 
 def sparse_backward(q, kv, o, do, lse, idx, sm_scale: Optional[float] = None, dv_dim: Optional[int] = None,
                     workspace=None, stream=None):
-    """dQ and dKV of top-k sparse attention over shared latent rows."""
+    """dQ and dKV of top-k sparse attention over shared latent rows: the
+    preprocess (no dQ accumulator, a dKV one), the sparse kernel, the dKV cast."""
     _dev(q, kv, o, do, lse, idx)
     B, S, H, DQK = q.shape
     SKV, HKV = kv.shape[1], kv.shape[2]
@@ -258,12 +259,12 @@ def sparse_backward(q, kv, o, do, lse, idx, sm_scale: Optional[float] = None, dv
         sm_scale = DQK ** -0.5
     dkv_elems = B * SKV * HKV * DQK
     if workspace is None:
-        workspace = new_workspace(B, S, H, DQK, dkv_elems, device=q.device)
+        workspace = new_workspace(B, S, H, 0, dkv_elems, device=q.device)
     dq = torch.empty_like(q)
     dkv = torch.empty_like(kv)
-    preprocess(o, do, lse, workspace, Dq=DQK, dkv_elems=dkv_elems, stream=stream)
-    attn_bwd_sparse(q, kv, do, idx, workspace, sm_scale, dv_dim, stream)
-    sparse_land(dq, dkv, workspace, stream)
+    preprocess(o, do, lse, workspace, Dq=0, dkv_elems=dkv_elems, stream=stream)
+    attn_bwd_sparse(q, kv, do, idx, dq, workspace, sm_scale, dv_dim, stream)
+    sparse_land(dkv, workspace, B, S, H, stream)
     return dq, dkv
 
 

@@ -83,6 +83,38 @@ bool make_acc_map(CUtensorMap* m, void* base, int64_t B, int64_t S, int64_t H, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over [B,S,H,Dfull] 16-bit with a box of 64 columns x 64 heads of
+// one token (the sparse path's Q and dO chunks), 128-byte swizzle.
+bool make_head_map(CUtensorMap* m, const void* base, attn_dtype_t dt, int64_t B, int64_t S, int64_t H, int64_t D,
+                   const attn_strides_t& st) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h * 2), static_cast<cuuint64_t>(st.s * 2),
+                           static_cast<cuuint64_t>(st.b * 2)};
+  cuuint32_t box[4] = {64, 64, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty = dt == ATTN_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, ty, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over ``rows`` dense rows of D 16-bit values, box 64 x 1 (for gather4).
+bool make_row_map(CUtensorMap* m, const void* base, attn_dtype_t dt, int64_t rows, int64_t D, int64_t row_stride) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride * 2)};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t es[2] = {1, 1};
+  const CUtensorMapDataType ty = dt == ATTN_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, ty, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uint64_t wait_limit_ns() { return ab::kWaitTimeoutNs; }
 
 }  // namespace
@@ -120,7 +152,7 @@ attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* 
                                   int64_t Dv, int64_t Dq, int64_t dkv_elems, attn_dtype_t dtype, void* workspace,
                                   size_t workspace_bytes, void* stream) {
   if (!o || !dO || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || H < 1 || Dv < 8 || Dv % 8 || Dv > 1024 || Dq < 8 || Dq % 8 || dkv_elems < 0)
+  if (B < 1 || S < 1 || H < 1 || Dv < 8 || Dv % 8 || Dv > 1024 || Dq < 0 || Dq % 8 || dkv_elems < 0)
     return ATTN_ERR_INVALID_ARG;
   if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
@@ -230,6 +262,73 @@ attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t 
   p.out = static_cast<uint8_t*>(dq);
   p.s_b = sdq.b, p.s_s = sdq.s, p.s_h = sdq.h;
   p.scale = sm_scale;
+  return launch_status(launch_land(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
+                              const void* dO, attn_strides_t sdo, const int32_t* idx, attn_strides_t sidx,
+                              int64_t B, int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV,
+                              int64_t topk, attn_dtype_t dtype, float sm_scale, void* dq, attn_strides_t sdq,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !kv || !dO || !idx || !dq || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || H % HKV != 0 || topk < 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  if (DQK != 576 || DV != 512 || H / HKV != 64) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (B * S * HKV >= (int64_t(1) << 31) || B * SKV * HKV >= (int64_t(1) << 31) || topk >= (int64_t(1) << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, kv, dO, static_cast<const void*>(idx), static_cast<const void*>(dq),
+                          static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  for (const attn_strides_t* st : {&sq, &sdo, &sdq})
+    if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
+  // the latent rows are gathered as rows of a dense [B*SKV*HKV, DQK] matrix
+  if (skv.h < DQK || (skv.h * 2) % 16 || skv.s != HKV * skv.h || skv.b != SKV * skv.s) return ATTN_ERR_UNSUPPORTED;
+  if (sidx.b < 0 || sidx.s < 0 || sidx.h < 0) return ATTN_ERR_INVALID_ARG;
+  const int64_t dkv_elems = B * SKV * HKV * DQK;
+  const WsLayout L = ws_layout(B, S, H, 0, dkv_elems);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  SparseMaps m;
+  if (!make_head_map(&m.q, q, dtype, B, S, H, DQK, sq) || !make_head_map(&m.dO, dO, dtype, B, S, H, DV, sdo) ||
+      !make_row_map(&m.kv, kv, dtype, B * SKV * HKV, DQK, skv.h))
+    return ATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SparseParams p{};
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.SKV = static_cast<int>(SKV);
+  p.H = static_cast<int>(H), p.HKV = static_cast<int>(HKV), p.topk = static_cast<int>(topk);
+  p.sm_scale = sm_scale;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
+  p.dkv_acc = reinterpret_cast<float*>(ws + L.dkv_off);
+  p.idx = idx;
+  p.si_b = sidx.b, p.si_s = sidx.s, p.si_h = sidx.h;
+  p.dq = static_cast<uint8_t*>(dq);
+  p.sdq_b = sdq.b, p.sdq_s = sdq.s, p.sdq_h = sdq.h;
+  p.err = &reinterpret_cast<WsHeader*>(ws)->err;
+  p.unit_counter = &reinterpret_cast<WsHeader*>(ws)->tile_counter;
+  p.timeout_ns = wait_limit_ns();
+  const int64_t units = B * S * HKV;
+  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  return launch_status(launch_sparse(p, m, dtype == ATTN_DT_BF16, grid, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd_sparse_land(void* dkv, attn_strides_t sdkv, int64_t B, int64_t S, int64_t SKV, int64_t H,
+                                   int64_t HKV, int64_t DQK, attn_dtype_t dtype, const void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!dkv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || DQK < 8 || DQK % 8) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(dkv) || !aligned16(workspace) || !strides_ok(sdkv)) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, S, H, 0, B * SKV * HKV * DQK);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  LandParams p{};
+  p.acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + L.dkv_off);
+  p.rows = B * SKV * HKV;
+  p.B = static_cast<int>(B), p.S = static_cast<int>(SKV), p.H = static_cast<int>(HKV), p.D = static_cast<int>(DQK);
+  p.out = static_cast<uint8_t*>(dkv);
+  p.s_b = sdkv.b, p.s_s = sdkv.s, p.s_h = sdkv.h;
+  p.scale = 1.f;
   return launch_status(launch_land(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
 }
 

@@ -55,6 +55,7 @@ enum DeviceError : int {
   kErrWaitKVFree = 0x10F,
   kErrWaitStage = 0x110,
   kErrWaitDKVFree = 0x111,
+  kErrAlign = 0x1FE,
   kErrSelftest = 0x1FF,
   kErrSparseBase = 0x200,
 };

@@ -57,6 +57,30 @@ struct DenseMaps {
   CUtensorMap dq;  // f32 dQ accumulator [B,S,HQ,D] (bulk reduce-add target)
 };
 
+struct SparseParams {
+  int B, S, SKV, H, HKV, topk;
+  float scale_log2;  // sm_scale * log2(e)
+  float sm_scale;
+  const float* lse2;   // [B,H,S]
+  const float* delta;  // [B,H,S]
+  float* dkv_acc;      // f32 [B,SKV,HKV,576]
+  const int* idx;      // [B,S,HKV,topk]
+  int64_t si_b, si_s, si_h;
+  uint8_t* dq;  // 16-bit [B,S,H,576]
+  int64_t sdq_b, sdq_s, sdq_h;
+  int* err;
+  int* unit_counter;
+  uint64_t timeout_ns;
+};
+
+struct SparseMaps {
+  CUtensorMap q;   // [B,S,H,576], box 64 d x 64 heads
+  CUtensorMap dO;  // [B,S,H,512], box 64 d x 64 heads
+  CUtensorMap kv;  // 2-D rows (b*SKV + j)*HKV + g of 576, box 64 x 1 (gather4)
+};
+
+cudaError_t launch_sparse(const SparseParams& p, const SparseMaps& m, bool bf16, int grid, cudaStream_t st);
+
 cudaError_t launch_preprocess(const PreprocessParams& p, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_land(const LandParams& p, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);

@@ -67,7 +67,7 @@ __device__ __forceinline__ void raise_error(const WaitCtx& c, int code) {
 }
 
 // Slow path of mbar_wait: bounded polling with abort and error checks.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
@@ -104,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
 
 // Last-resort drain used on the abort path: waits (bounded, without consulting
 // the abort flag) for a phase whose producer is known to be in flight.
-__device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+static __device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
   while (!mbar_try(bar, parity)) {
     if (global_ns() - t0 > kWaitTimeoutNs) return;
@@ -146,6 +146,26 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* m, int c0,
 }
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+// Gather of four rows (row coordinates r0..r3, any of them out of range reads
+// zeros) of a 2-D tensor whose box is one row high, 64 columns from c0; the
+// rows land consecutively at dst with the map's swizzle.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int r0, int r1,
+                                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+// Element-wise f32 add of ``bytes`` contiguous bytes of shared memory into
+// global memory (both 16-byte aligned, size a multiple of 16), bulk-group
+// completion.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
 }
 // Plain (untensored) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.

@@ -103,7 +103,8 @@ ATTN_BWD_API size_t attn_bwd_workspace_size(int64_t B, int64_t S, int64_t H, int
  * preprocess of the TileOPs page ("delta_rows" in its Base and Tiled
  * programs).
  *   o, dO : [B,S,H,Dv] 16-bit;  lse : f32, lse[b*slse.b + h*slse.h + s*slse.s]
- *   Dq    : head dim of Q (sizes the dQ accumulator); dkv_elems as above.
+ *   Dq    : head dim of Q (sizes the dQ accumulator; 0 for the sparse path,
+ *           which needs none); dkv_elems as above.
  * Dv must be a multiple of 8 and at most 1024. */
 ATTN_BWD_API attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
                                   const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t H,
@@ -140,28 +141,32 @@ ATTN_BWD_API attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_
 /* Launch 2, top-k sparse attention over shared latent rows (the tilelang
  * sparse MLA backward): query t of batch b, head h (KV head g = h / (H/HKV))
  * attends the latent rows kv[b, idx[b,t,g,s], g, :] for every slot s whose
- * index lies in [0, SKV) (-1 pads).  K is the whole DQK-wide row, V its first
- * DV columns.  Adds dQ partials into the workspace dQ accumulator and
- * dKV = dK + [dV, 0] partials into the workspace dKV accumulator
- * (dkv_elems = B*SKV*HKV*DQK at preprocess time).
- *   q : [B,S,H,DQK];  kv : [B,SKV,HKV,DQK];  dO : [B,S,H,DV] 16-bit
+ * index lies in [0, SKV); other entries (-1 pads) are not visible.  K is the
+ * whole DQK-wide row, V its first DV columns.  One CTA owns a (token, KV
+ * head) pair with all of its query heads, so dQ (which already includes
+ * sm_scale) is written here, once; dKV = dK + [dV, 0] partials are added into
+ * the workspace's f32 dKV accumulator, which attn_bwd_sparse_land casts.
+ * The preprocess before it runs with Dq = 0 (no dQ accumulator) and
+ * dkv_elems = B*SKV*HKV*DQK.
+ *   q, dq : [B,S,H,DQK];  kv : [B,SKV,HKV,DQK] stored densely (row stride
+ *   DQK); dO : [B,S,H,DV] 16-bit
  *   idx : int32 [B,S,HKV,topk] with strides sidx (slot stride 1)
- *   DQK = 576, DV = 512;  H / HKV a multiple of 64;  topk a multiple of 64. */
+ *   DQK = 576, DV = 512;  H / HKV = 64;  topk >= 1. */
 ATTN_BWD_API attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
-                              const void* dO, attn_strides_t sdo, const int32_t* idx, attn_strides_t sidx,
-                              int64_t B, int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV,
-                              int64_t topk, attn_dtype_t dtype, float sm_scale, void* workspace,
-                              size_t workspace_bytes, void* stream);
+                                           const void* dO, attn_strides_t sdo, const int32_t* idx,
+                                           attn_strides_t sidx, int64_t B, int64_t S, int64_t SKV, int64_t H,
+                                           int64_t HKV, int64_t DQK, int64_t DV, int64_t topk, attn_dtype_t dtype,
+                                           float sm_scale, void* dq, attn_strides_t sdq, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
-/* Launch 3 of the sparse path: dQ = cast(dQacc) and dKV = cast(dKVacc).
- * (The sparse kernel applies sm_scale to dS itself: dKV mixes the scaled dK
- * term with the unscaled dV term, so the scale cannot be folded into the
- * landing pass as on the dense path.)
- *   dq : [B,S,H,DQK];  dkv : [B,SKV,HKV,DQK] 16-bit (written). */
-ATTN_BWD_API attn_status_t attn_bwd_sparse_land(void* dq, attn_strides_t sdq, void* dkv, attn_strides_t sdkv, int64_t B,
-                                   int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK,
-                                   attn_dtype_t dtype, const void* workspace, size_t workspace_bytes,
-                                   void* stream);
+/* Launch 3 of the sparse path: dKV = cast(dKVacc) (the sparse kernel applies
+ * sm_scale to dS itself: dKV mixes the scaled dK term with the unscaled dV
+ * term, so the scale cannot be folded into a landing pass as on the dense
+ * path).  B, S, H locate the workspace regions as at preprocess time.
+ *   dkv : [B,SKV,HKV,DQK] 16-bit (written). */
+ATTN_BWD_API attn_status_t attn_bwd_sparse_land(void* dkv, attn_strides_t sdkv, int64_t B, int64_t S, int64_t SKV,
+                                                int64_t H, int64_t HKV, int64_t DQK, attn_dtype_t dtype,
+                                                const void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises ``stream`` and reports the device error word of ``workspace``:
  * ATTN_OK, ATTN_ERR_TIMEOUT (a bounded wait ran out; *device_code, if not

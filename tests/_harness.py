@@ -95,3 +95,42 @@ def assert_close(got, ref, w, what):
         raise AssertionError(f"{what}: {int(bad.sum())} of {int(m.sum())} elements out of tolerance "
                              f"(max err {err[m].max():.3e}); e.g. {detail}")
     return float(err[m].max())
+
+
+@functools.lru_cache(maxsize=2)
+def sparse_problem(w, idx_override=None):
+    """Inputs of a sparse workload plus O and LSE from the oracle's float32 forward."""
+    q, kv, do, idx = inputs.sparse_inputs(w)
+    if idx_override is not None:
+        idx = np.array(idx_override, dtype=np.int32).reshape(idx.shape)
+    o, lse = oracle.sparse_forward(q, kv, idx, w.sm_scale, w.Dv)
+    o = inputs.round_to_dtype(o, w.dtype)
+    return q, kv, do, idx, o, np.ascontiguousarray(lse, dtype=np.float32)
+
+
+def run_sparse(w, problem, poison=True):
+    """The sparse path's three launches through the binding, outputs NaN-poisoned."""
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    q, kv, do, idx, o, lse = problem
+    dt = torch_dtype(w)
+    t = lambda a: torch.from_numpy(a).cuda().to(dt)  # noqa: E731
+    tq, tkv, tdo, to = t(q), t(kv), t(do), t(o)
+    tidx = torch.from_numpy(idx).cuda()
+    tl = torch.from_numpy(lse).cuda()
+    B, S, H, DQK = q.shape
+    SKV, HKV = kv.shape[1], kv.shape[2]
+    dkv_elems = B * SKV * HKV * DQK
+    ws = ab._binding.new_workspace(B, S, H, 0, dkv_elems)
+    if poison:
+        ws.fill_(0xFF)
+    fill = float("nan") if poison else 0.0
+    dq = torch.full_like(tq, fill)
+    dkv = torch.full_like(tkv, fill)
+    ab.preprocess(to, tdo, tl, ws, Dq=0, dkv_elems=dkv_elems)
+    ab.attn_bwd_sparse(tq, tkv, tdo, tidx, dq, ws, w.sm_scale, w.Dv)
+    ab.sparse_land(dkv, ws, B, S, H)
+    ab.check_error(ws)
+    return dq, dkv
