@@ -339,16 +339,35 @@ def sparse_backward(q, kv, o, do, lse, idx, scale, dv_dim, tokens=None, kv_rows=
                     np.add.at(dkv[b, :, g, :], r["sl"], r["dkv"])
 
     if rows_wanted is not None:
-        for b in range(B):
-            for g in range(HKV):
-                for j in rows_wanted:
-                    acc = np.zeros(DQK)
-                    # every (token, slot) that lists row j
-                    toks_j = np.nonzero((idx[b, :, g, :] == j).any(axis=1))[0]
-                    for t in toks_j:
-                        sl, Kt, Qt, dOt, P, dS = token_grads(b, int(t), g)
-                        for s_i in np.nonzero(sl == j)[0]:
-                            acc += dS[:, s_i] @ Qt
-                            acc[:dv_dim] += P[:, s_i] @ dOt
-                    dkv[b, j, g, :] = acc
+        # dKV[j] = sum over the (token, slot) pairs that list row j of
+        # dS[:, slot]^T Q_t (+ P[:, slot]^T dO_t on the value columns); P and dS
+        # of such a slot need only row j itself and the token's LSE and delta.
+        dlt_all = (o.astype(np.float64) * do.astype(np.float64)).sum(axis=-1)  # [B,S,H]
+
+        def row_grad(b, g, j):
+            hs = slice(g * G, (g + 1) * G)
+            lists = idx[b, :, g, :]
+            mult = (lists == j).sum(axis=1)          # a repeated index is a separate slot
+            toks_j = np.nonzero(mult)[0]
+            acc = np.zeros(DQK)
+            if j < 0 or j >= SKV or toks_j.size == 0:
+                return b, g, j, acc
+            Kj = kv[b, j, g, :].astype(np.float64)
+            for c0 in range(0, toks_j.size, 256):
+                tt = toks_j[c0:c0 + 256]
+                Qt = q[b, tt][:, hs, :].astype(np.float64)       # [n, G, DQK]
+                dOt = do[b, tt][:, hs, :].astype(np.float64)     # [n, G, DV]
+                L = lse[b, hs][:, tt].T.astype(np.float64)       # [n, G]
+                P = np.exp(scale * (Qt @ Kj) - L)                # [n, G]
+                dP = dOt @ Kj[:dv_dim]
+                dS = P * (dP - dlt_all[b, tt][:, hs]) * scale
+                m = mult[tt].astype(np.float64)[:, None]
+                acc += np.einsum("ng,ngd->d", dS * m, Qt)
+                acc[:dv_dim] += np.einsum("ng,ngd->d", P * m, dOt)
+            return b, g, j, acc
+
+        jobs = [(b, g, int(j)) for b in range(B) for g in range(HKV) for j in rows_wanted]
+        with ThreadPoolExecutor(_threads()) as ex:
+            for b, g, j, acc in ex.map(lambda a: row_grad(*a), jobs):
+                dkv[b, j, g, :] = acc
     return dq, dkv

@@ -234,6 +234,17 @@ def test_row_subsets_equal_full_evaluation():
     np.testing.assert_allclose(dkv_rows[0, [0, 4, 9]], dkvs[0, [0, 4, 9]], rtol=1e-12, atol=1e-14)
     dq_t, _ = oracle.sparse_backward(qs, kvs, os_, dos, ls, idx, 0.5, 3, tokens=[2, 8])
     np.testing.assert_allclose(dq_t[0, [2, 8]], dqs[0, [2, 8]], rtol=1e-12, atol=1e-14)
+    # two KV groups, a repeated index, an out-of-range index and -1 padding
+    idx2 = np.stack([inputs.topk_index_sets(5, g, 10, 5) for g in range(2)], axis=1)[None]
+    idx2[0, 6, 0, 1] = idx2[0, 6, 0, 0]
+    idx2[0, 7, 1, 2] = 12
+    idx2[0, 9, 1, :] = -1
+    qs, kvs, dos = _rand(rng, 1, 10, 4, 4), _rand(rng, 1, 10, 2, 4), _rand(rng, 1, 10, 4, 3)
+    os_, ls = oracle.sparse_forward(qs, kvs, idx2, 0.5, 3, dtype=np.float64)
+    _, dkvs = oracle.sparse_backward(qs, kvs, os_, dos, ls, idx2, 0.5, 3)
+    rows = [0, int(idx2[0, 6, 0, 0]), 5, 9]
+    _, dkv_rows = oracle.sparse_backward(qs, kvs, os_, dos, ls, idx2, 0.5, 3, kv_rows=rows)
+    np.testing.assert_allclose(dkv_rows[0, rows], dkvs[0, rows], rtol=1e-12, atol=1e-14)
 
 
 def test_delta_is_rowwise_dot():
