@@ -102,9 +102,24 @@ def round_to_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f16":
         return x.astype(np.float16).astype(np.float32)
     if dtype == "bf16":
-        u = x.view(np.uint32).astype(np.uint64)
-        u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) & np.uint64(0xFFFF0000)
-        return u.astype(np.uint32).view(np.float32).reshape(x.shape)
+        # RNE on the bit pattern: add 0x7FFF plus the lowest kept bit, then
+        # truncate.  For finite values the sum stays below 2^32; NaNs are kept.
+        u = x.reshape(-1).view(np.uint32).copy()
+
+        def rne(a, e):
+            c = u[a:e]
+            lsb = (c >> np.uint32(16)) & np.uint32(1)
+            nan = (c & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+            keep = c[nan]
+            c += np.uint32(0x7FFF)
+            c += lsb
+            c &= np.uint32(0xFFFF0000)
+            c[nan] = keep
+
+        step = 1 << 22
+        with ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1))) as ex:
+            list(ex.map(lambda a: rne(a, min(a + step, u.size)), range(0, u.size, step)))
+        return u.view(np.float32).reshape(x.shape)
     if dtype == "f32":
         return x
     raise ValueError(f"unknown dtype {dtype}")
