@@ -31,9 +31,11 @@
 // as the previous block's last reader of the slot block (dQ^T) has been issued
 // (the Little's-law argument of the tilelang page, "Mechanism").
 //
-// Warp roles (10 warps): 0-3 dKV epilogue (lane = slot), 4-7 softmax/dS
-// (lane = slot, all 64 heads) and the token's dQ output, 8 producer (unit
-// scheduling, index lists, gathers, Q/dO ring), 9 MMA issuer.  Every wait is
+// Warp roles (11 warps): 0-3 dKV epilogue (lane = slot), 4-7 softmax/dS
+// (lane = slot, all 64 heads) and the token's dQ output, 8 Q/dO ring
+// producer, 9 MMA issuer, 10 unit scheduling, index lists and gathers (a warp
+// of its own, so that the next block's gather is issued the moment dQ^T frees
+// the slot block instead of queueing behind the ring loads).  Every wait is
 // bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -80,7 +82,7 @@ constexpr int T_DQ = 0;     // five dQ^T tiles [128 d x 64 heads] at 64-column s
 constexpr int T_S = 320;    // S^T [128 slots x 64 heads] f32; then P^T hi (upper 32) and lo (lower 32) pairs
 constexpr int T_DP = 384;   // dP^T f32; then dS^T hi (upper 32) and lo (lower 32) pairs
 constexpr int T_DKV = 448;  // one dKV chunk [128 slots x 64 cols] f32
-constexpr int THREADS = 10 * 32;
+constexpr int THREADS = 11 * 32;
 
 enum Bar : int {
   RING_FULL0 = 0,   // 3
@@ -103,8 +105,9 @@ enum Bar : int {
 };
 static_assert(NUM_BARS <= NBAR, "barrier storage");
 
+// 168 registers: three warps of one SM sub-partition must fit its 16K registers.
 template <bool BF16>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __maxnreg__(168)
     sparse_bwd_kernel(const __grid_constant__ SparseMaps maps, const SparseParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bars[KV_FREE], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[UNIT_FULL0 + i], 1);
-      mbar_init(&bars[UNIT_EMPTY0 + i], 9);  // MMA warp + 4 softmax warps + 4 epilogue warps
+      mbar_init(&bars[UNIT_EMPTY0 + i], 10);  // ring producer, MMA warp, 4 softmax warps, 4 epilogue warps
     }
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[DP_FULL], 1);
@@ -154,11 +157,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int units_total = p.B * p.S * p.HKV;
 
-  if (warp == 8) {
-    // ============================================================ producer
+  if (warp == 10) {
+    // ============================================================ units, index lists, gathers
     int kv_pend[2] = {-1, -1};
-    int ring_pend[RING] = {-1, -1, -1};
-    uint32_t gb = 0, rc = 0;
+    uint32_t gb = 0;
     bool ok = true;
     for (int uc = 0; ok; ++uc) {
       const int slot = uc & 1;
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!valid) break;
       const int* il = p.idx + b * p.si_b + static_cast<int64_t>(t) * p.si_s + g * p.si_h;
       for (int blk = 0; blk < nb && ok; ++blk, ++gb) {
-        // ---- gather the block's latent rows once the previous block's dQ^T is done with the slot block
+        // the block's latent rows, once the previous block's dQ^T is done with the slot block
         if (gb >= 1 && !(ok = mbar_wait_warp(&bars[KV_FREE], (gb - 1) & 1, wc, kErrSparseBase + 2))) break;
         int* ib = idx_buf + (gb & 1) * BK;
         int rows[4];
@@ -217,8 +219,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < NSK; ++s)
           tma_gather4(sm + OFF_KV + s * SLAB + lane * 512, &maps.kv, &bars[KV_FULL0 + (gb & 1)], s * 64, rows[0],
                       rows[1], rows[2], rows[3]);
-        kv_pend[gb & 1] = (gb >> 1) & 1;
-        // ---- the block's Q/dO chunks, in the MMA's order, twice
+        if (gb & 1) kv_pend[1] = (gb >> 1) & 1; else kv_pend[0] = (gb >> 1) & 1;
+      }
+    }
+    if (lane == 0) {  // gathers in flight land before the CTA exits
+      if (kv_pend[0] >= 0) mbar_drain(&bars[KV_FULL0], kv_pend[0]);
+      if (kv_pend[1] >= 0) mbar_drain(&bars[KV_FULL0 + 1], kv_pend[1]);
+    }
+  } else if (warp == 8) {
+    // ============================================================ Q/dO ring producer
+    uint32_t ring_used = 0, ring_par = 0;  // per ring slot: loaded at least once, parity of its last load
+    uint32_t rc = 0;
+    bool ok = true;
+    for (int uc = 0; ok; ++uc) {
+      const int slot = uc & 1;
+      if (!(ok = mbar_wait_warp(&bars[UNIT_FULL0 + slot], (uc >> 1) & 1, wc, kErrSparseBase + 21))) break;
+      const int valid = units[slot].valid, nb = units[slot].nb, b = units[slot].b, t = units[slot].t,
+                g = units[slot].g;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[UNIT_EMPTY0 + slot]);
+      if (!valid) break;
+      for (int blk = 0; blk < nb && ok; ++blk) {
+        // the block's Q/dO chunks, in the MMA's order, twice
         for (int pass = 0; pass < 2 && ok; ++pass) {
           for (int i = 0; i < NCHUNK; ++i, ++rc) {
             const int rs = rc % RING;
@@ -232,16 +254,15 @@ __global__ void __launch_bounds__(THREADS, 1)
               tma_load_4d(sm + OFF_RING + rs * CHUNK, isq ? &maps.q : &maps.dO, &bars[RING_FULL0 + rs], c * 64, g * SH,
                           t, b);
             }
-            ring_pend[rs] = (rc / RING) & 1;
+            ring_used |= 1u << rs;
+            ring_par = (ring_par & ~(1u << rs)) | (((rc / RING) & 1u) << rs);
           }
         }
       }
     }
-    if (lane == 0) {  // copies in flight land before the CTA exits
-      for (int i = 0; i < 2; ++i)
-        if (kv_pend[i] >= 0) mbar_drain(&bars[KV_FULL0 + i], kv_pend[i]);
+    if (lane == 0) {  // ring loads in flight land before the CTA exits
       for (int i = 0; i < RING; ++i)
-        if (ring_pend[i] >= 0) mbar_drain(&bars[RING_FULL0 + i], ring_pend[i]);
+        if ((ring_used >> i) & 1u) mbar_drain(&bars[RING_FULL0 + i], (ring_par >> i) & 1u);
     }
   } else if (warp == 9) {
     // ============================================================ MMA issuer (whole warp, one elected lane)
@@ -421,7 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const int d = 128 * m + row;
         if (d < DQK) {
-#pragma unroll 8
+#pragma unroll
           for (int h = 0; h < SH; ++h) {
             const uint32_t w = pack2<BF16>(__uint_as_float(r[h]), 0.f);
             *reinterpret_cast<uint16_t*>(dq + 2 * (h * p.sdq_h + d)) = static_cast<uint16_t>(w & 0xffffu);

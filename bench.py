@@ -67,6 +67,24 @@ def sparse_flops(w, idx) -> float:
     return valid * w.HQ * 2.0 * (3 * w.D + 2 * w.Dv)
 
 
+def sparse_valid_pairs(w, idx) -> int:
+    return int(((idx >= 0) & (idx < w.S)).sum())
+
+
+def sparse_hbm_bytes(w, idx):
+    """Algorithmic DRAM bytes of each launch of the sparse path: every input and
+    output crosses HBM once (the gathered latent rows come from L2: KV is read
+    from DRAM once), the f32 dKV accumulator is read and written once by the
+    scatter and read once by the landing pass."""
+    B, S, H, HKV, DQK, DV, K = w.B, w.S, w.HQ, w.HKV, w.D, w.Dv, w.topk
+    SKV = w.S
+    pre = B * S * H * DV * 2 * 2 + B * H * S * 4 + B * S * H * 4 * 2 + B * SKV * HKV * DQK * 4
+    main = (B * S * H * DQK * 2 * 2 + B * S * H * DV * 2 + B * S * H * 4 * 2 + B * S * HKV * K * 4
+            + B * SKV * HKV * DQK * 2 + B * SKV * HKV * DQK * 4 * 2)
+    land = B * SKV * HKV * DQK * (4 + 2)
+    return {"preprocess": pre, "main": main, "land": land, "gathered_l2": sparse_valid_pairs(w, idx) * DQK * 2}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
 
@@ -176,9 +194,73 @@ def gpu_dense_inputs(w, device):
     return tq, tk, tv, o, tdo, lse
 
 
+def gpu_sparse_inputs(w, device):
+    """Q, KV, dO and the index lists from the seeded generator; O and LSE from a
+    float32 torch forward over the listed rows on the device (not timed)."""
+    import torch
+
+    from attention_backward_gb300 import inputs
+
+    q, kv, do, idx = inputs.sparse_inputs(w)
+    tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    tq, tkv, tdo = (torch.from_numpy(a).to(device).to(tdt) for a in (q, kv, do))
+    tidx = torch.from_numpy(idx).to(device)
+    G = w.HQ // w.HKV
+    o = torch.empty_like(tdo)
+    lse = torch.empty(w.B, w.HQ, w.S, dtype=torch.float32, device=device)
+    for b in range(w.B):
+        for g in range(w.HKV):
+            hs = slice(g * G, (g + 1) * G)
+            for t0 in range(0, w.S, 128):
+                t1 = min(w.S, t0 + 128)
+                ix = tidx[b, t0:t1, g].long()
+                ok = (ix >= 0) & (ix < w.S)
+                rows = tkv[b, ix.clamp(0, w.S - 1), g].float()            # [T, topk, DQK]
+                s_ = torch.einsum("thd,tkd->thk", tq[b, t0:t1, hs].float(), rows) * w.sm_scale
+                s_ = s_.masked_fill(~ok[:, None, :], float("-inf"))
+                l_ = torch.logsumexp(s_, dim=2)
+                o[b, t0:t1, hs] = torch.einsum("thk,tkd->thd", torch.exp(s_ - l_[..., None]),
+                                               rows[..., :w.Dv]).to(tdt)
+                lse[b, hs, t0:t1] = l_.T
+    return tq, tkv, o, tdo, lse, tidx, idx
+
+
 # ------------------------------------------------------------------ GPU arm
 
-def time_dense(w, steps, warmup, device, flush_bytes=256 << 20):
+def _timed_steps(step, steps, warmup, device, stream, ws, nev, flush_bytes, world):
+    """W untimed steps, then K steps each bracketed by CUDA events on the
+    launching stream, L2 flushed (a write larger than L2) before each; a barrier
+    and a device synchronisation on both sides of the timed region."""
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=device)
+    for _ in range(warmup):
+        flush.zero_()
+        step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
+    ab.check_error(ws, stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+        step(ev)
+        per.append(ev)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    ab.check_error(ws, stream)
+    return per
+
+def time_dense(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
     import torch
 
     import attention_backward_gb300 as ab
@@ -187,66 +269,85 @@ def time_dense(w, steps, warmup, device, flush_bytes=256 << 20):
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=device) if w.cu_seqlens else None
     ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
     dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
-    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step():
+    def step(ev):
+        ev[0].record(stream)
         ab.preprocess(to, tdo, lse, ws, Dq=w.D, stream=stream)
         ev[1].record(stream)
         ab.attn_bwd_gqa(tq, tk, tv, tdo, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
         ev[2].record(stream)
         ab.dq_land(dq, ws, w.sm_scale, stream)
+        ev[3].record(stream)
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    for _ in range(warmup):
-        flush.zero_()
+    per = _timed_steps(step, steps, warmup, device, stream, ws, 4, flush_bytes, world)
+    return _stage_times(per) | {"tensors": (tq, tk, tv, to, tdo, lse, cu)}
+
+
+def time_sparse(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    tq, tkv, to, tdo, lse, tidx, idx = gpu_sparse_inputs(w, device)
+    dkv_elems = tkv.numel()
+    ws = ab._binding.new_workspace(w.B, w.S, w.HQ, 0, dkv_elems, device=device)
+    dq, dkv = torch.empty_like(tq), torch.empty_like(tkv)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev):
         ev[0].record(stream)
-        step()
+        ab.preprocess(to, tdo, lse, ws, Dq=0, dkv_elems=dkv_elems, stream=stream)
+        ev[1].record(stream)
+        ab.attn_bwd_sparse(tq, tkv, tdo, tidx, dq, ws, w.sm_scale, w.Dv, stream)
+        ev[2].record(stream)
+        ab.sparse_land(dkv, ws, w.B, w.S, w.HQ, stream)
         ev[3].record(stream)
-    ab.check_error(ws, stream)
-    torch.cuda.synchronize(device)
-    per = []
-    for _ in range(steps):
-        flush.zero_()  # L2 flush between timed steps (256 MiB write > 129 MB L2)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        ev[0].record(stream)
-        step()
-        ev[3].record(stream)
-        per.append(ev)
-    torch.cuda.synchronize(device)
-    ab.check_error(ws, stream)
+
+    per = _timed_steps(step, steps, warmup, device, stream, ws, 4, flush_bytes, world)
+    return _stage_times(per) | {"tensors": (tq, tkv, to, tdo, lse, tidx), "idx": idx}
+
+
+def _stage_times(per):
     tot = [e[0].elapsed_time(e[3]) for e in per]
-    pre = [e[0].elapsed_time(e[1]) for e in per]
-    main = [e[1].elapsed_time(e[2]) for e in per]
-    land = [e[2].elapsed_time(e[3]) for e in per]
-    return {"ms_step": float(np.mean(tot)), "ms_pre": float(np.mean(pre)), "ms_main": float(np.mean(main)),
-            "ms_land": float(np.mean(land)), "ms_step_median": float(np.median(tot)),
-            "tensors": (tq, tk, tv, to, tdo, lse, cu)}
+    return {"ms_step": float(np.mean(tot)), "ms_step_median": float(np.median(tot)),
+            "ms_pre": float(np.mean([e[0].elapsed_time(e[1]) for e in per])),
+            "ms_main": float(np.mean([e[1].elapsed_time(e[2]) for e in per])),
+            "ms_land": float(np.mean([e[2].elapsed_time(e[3]) for e in per]))}
 
 
 def time_e2e(w, tensors, steps, device):
     """The same backward through the public API with pinned host buffers:
-    host->device copies of the inputs and device->host copies of dQ, dK, dV
+    host->device copies of the inputs and device->host copies of the gradients
     inside the timed region."""
     import torch
 
     import attention_backward_gb300 as ab
 
-    tq, tk, tv, to, tdo, lse, cu = tensors
-    host_in = [t.cpu().pin_memory() for t in (tq, tk, tv, to, tdo, lse)]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (tq, tk, tv)]
+    stream = torch.cuda.current_stream(device)
+    if w.kind == "sparse":
+        host_in = [t.cpu().pin_memory() for t in tensors]           # q, kv, o, do, lse, idx
+        outs = (tensors[0], tensors[1])                             # dq like q, dkv like kv
+        ws = ab._binding.new_workspace(w.B, w.S, w.HQ, 0, tensors[1].numel(), device=device)
+    else:
+        host_in = [t.cpu().pin_memory() for t in tensors[:6]]       # q, k, v, o, do, lse
+        outs = tensors[:3]
+        ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
+        cu = tensors[6]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    stream = torch.cuda.current_stream(device)
-    ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
     dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_in]
 
     def one():
         for d, h in zip(dev_in, host_in):
             d.copy_(h, non_blocking=True)
-        dq, dk, dv = ab.backward(*dev_in, w.sm_scale, causal=w.causal, window=w.window, cu_seqlens=cu,
-                                 workspace=ws, stream=stream)
-        for h, d in zip(host_out, (dq, dk, dv)):
+        if w.kind == "sparse":
+            grads = ab.sparse_backward(*dev_in, w.sm_scale, w.Dv, workspace=ws, stream=stream)
+        else:
+            grads = ab.backward(*dev_in, w.sm_scale, causal=w.causal, window=w.window, cu_seqlens=cu,
+                                workspace=ws, stream=stream)
+        for h, d in zip(host_out, grads):
             h.copy_(d, non_blocking=True)
 
     one()
@@ -332,14 +433,75 @@ def run_reference(args):
     return 0
 
 
+def describe(w, r, pk, pk_kind, world=1):
+    """Throughput, roofline and per-stage figures of one timed workload."""
+    import os as _os
+
+    ms, ms_main = r["ms_step"], r["ms_main"]
+    csrc = _os.path.join(ROOT, "attention_backward_gb300", "csrc")
+    if w.kind == "sparse":
+        idx = r["idx"]
+        flops = sparse_flops(w, idx)
+        by = sparse_hbm_bytes(w, idx)
+        step_bytes = by["preprocess"] + by["main"] + by["land"]
+        kname = f"sparse_bwd_kernel<{w.dtype}>"
+        t_tensor = flops / (float(pk["bf16_tflops"]) * 1e12)
+        t_hbm = by["main"] / (float(pk["hbm_gbs"]) * 1e9)
+        out = {"value": step_bytes * world / (ms * 1e-3) / 1e9, "unit": "GB/s",
+               "TFLOP/s": flops * world / (ms * 1e-3) / 1e12,
+               "valid_pairs": sparse_valid_pairs(w, idx), "algorithmic_bytes": by}
+        achieved_t = flops / (ms_main * 1e-3) / 1e12
+        achieved_b = by["main"] / (ms_main * 1e-3) / 1e9
+        tensor_roof = {"bound": "tensor", "achieved": achieved_t, "peak": float(pk["bf16_tflops"]),
+                       "unit": "TFLOP/s", "frac": achieved_t / float(pk["bf16_tflops"])}
+        hbm_roof = {"bound": "hbm", "achieved": achieved_b, "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                    "frac": achieved_b / float(pk["hbm_gbs"])}
+        roof = dict(tensor_roof if t_tensor >= t_hbm else hbm_roof)
+        roof["other_bound"] = hbm_roof if t_tensor >= t_hbm else tensor_roof
+        roof["l2_gather_GB/s"] = by["gathered_l2"] / (ms_main * 1e-3) / 1e9
+        src = _os.path.join(csrc, "sparse_bwd.cu")
+    else:
+        flops = dense_flops(w)
+        out = {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s"}
+        achieved = flops / (ms_main * 1e-3) / 1e12
+        peak = float(pk["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+        kname = f"dense_bwd_kernel<{w.D},{w.dtype}>"
+        src = _os.path.join(csrc, "dense_bwd.cu")
+    roof["traffic"] = traffic_record(src, kname + "@" + w.name)
+    roof["peak_kind"] = f"{'bf16 burst' if roof['bound'] == 'tensor' else 'copy'}, {pk_kind}"
+    roof["kernel"] = kname
+    roof["kernel_ms"] = ms_main
+    out["roofline"] = roof
+    out["stages_ms"] = {"preprocess": r["ms_pre"], "main": ms_main, "land": r["ms_land"]}
+    out["ms_per_step"] = ms
+    return out, flops
+
+
+def workload_config(w):
+    c = {"workload": w.name, "B": w.B, "S": w.S, "HQ": w.HQ, "HKV": w.HKV, "D": w.D, "causal": w.causal,
+         "sm_scale": w.sm_scale}
+    if w.kind == "sparse":
+        c.update({"DV": w.Dv, "topk": w.topk})
+    if w.window > 0:
+        c["window"] = w.window
+    if w.cu_seqlens is not None:
+        c["cu_seqlens"] = list(w.cu_seqlens)
+    c["l2"] = "flushed before every step (256 MiB write)"
+    c["timed"] = "preprocess + main + landing per step"
+    return c
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=MAIN_WORKLOAD, help="workload of the main line (profiling)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -356,52 +518,46 @@ def main():
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    w = inputs.WORKLOADS[MAIN_WORKLOAD]
+    w = inputs.WORKLOADS[args.workload]
     pk, pk_kind = peaks()
+    timer = time_sparse if w.kind == "sparse" else time_dense
 
     clocks = ClockSampler(local)
     clocks.start()
-    r = time_dense(w, args.steps, args.warmup, device)
+    r = timer(w, args.steps, args.warmup, device, world)
     clk = clocks.stop()
-    ms = r["ms_step"]
     if world > 1:
         import torch.distributed as dist
 
-        t = torch.tensor([ms, r["ms_main"]], device=device)
+        t = torch.tensor([r["ms_step"], r["ms_main"]], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_main = float(t[0]), float(t[1])
-    else:
-        ms_main = r["ms_main"]
-    flops = dense_flops(w)
-    value = flops * world / (ms * 1e-3) / 1e12
-    e2e_ms, h2d, d2h = time_e2e(w, r["tensors"], max(3, args.steps // 4), device)
-    peak = float(pk["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
-    achieved = flops / (ms_main * 1e-3) / 1e12
-    traffic = traffic_record(os.path.join(ROOT, "attention_backward_gb300", "csrc", "dense_bwd.cu"),
-                             "dense_bwd_kernel<128,f16>@" + MAIN_WORKLOAD)
+        r["ms_step"], r["ms_main"] = float(t[0]), float(t[1])
+    d, flops = describe(w, r, pk, pk_kind, world)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": MAIN_WORKLOAD, "B": w.B, "S": w.S, "H": w.HQ, "D": w.D, "causal": True,
-                   "sm_scale": w.sm_scale, "l2": "flushed before every step (256 MiB write)",
-                   "timed": "preprocess + main + dQ landing per step"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_kind": f"bf16 burst, {pk_kind}",
-                     "kernel": "dense_bwd_kernel<128,f16>", "kernel_ms": ms_main},
-        "stages_ms": {"preprocess": r["ms_pre"], "main": r["ms_main"], "dq_land": r["ms_land"]},
-        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clk,
+        "metric": METRIC, "value": d["value"], "unit": d["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w),
+        "roofline": d["roofline"], "stages_ms": d["stages_ms"],
     }
+    if w.kind == "sparse":
+        line["TFLOP/s"] = d["TFLOP/s"]
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(w, r["tensors"], max(3, args.steps // 4), device)
+        per_step = d["value"] * r["ms_step"] / world  # this rank's units per step
+        line["e2e"] = {"value": per_step * world / e2e_ms, "unit": d["unit"], "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    else:
+        line["e2e"] = None
+    line["gpu_launches"] = 3 * args.steps
+    line["clocks"] = clk
     del r
+    torch.cuda.empty_cache()
     if not args.no_extra and world == 1:
-        line["workloads"] = extra_workloads(max(5, args.steps // 2), args.warmup, device, pk)
-    if not args.no_cpu and world == 1 and rank == 0:
+        line["workloads"] = extra_workloads(w.name, max(5, args.steps // 2), args.warmup, device, pk, pk_kind)
+    if not args.no_cpu and world == 1 and rank == 0 and w.kind == "dense":
         cv, el, nh = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": cv, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": f"{nh} of {w.HQ} query heads x {w.B} batch rows of {MAIN_WORKLOAD}, "
+                                "sample": f"{nh} of {w.HQ} query heads x {w.B} batch rows of {w.name}, "
                                           f"{el:.1f} s of float64 numpy"}
     else:
         line["cpu_baseline"] = None
@@ -415,19 +571,19 @@ def main():
     return 0
 
 
-def extra_workloads(steps, warmup, device, pk):
-    """The other dense workloads, same timing method (context for the roofline)."""
+def extra_workloads(main_name, steps, warmup, device, pk, pk_kind):
+    """The other workloads, same timing method, each with its own roofline."""
     import torch
 
     from attention_backward_gb300 import inputs
 
     out = {}
-    for name in ("gqa_1x16384_hq32_hkv4_d128_bf16", "gqa_varlen_window1024_hq32_hkv8_d64_bf16"):
-        w = inputs.WORKLOADS[name]
-        r = time_dense(w, steps, warmup, device)
-        f = dense_flops(w)
-        out[name] = {"ms_per_step": r["ms_step"], "TFLOP/s": f / (r["ms_step"] * 1e-3) / 1e12,
-                     "main_ms": r["ms_main"], "main_frac_of_peak": f / (r["ms_main"] * 1e-3) / 1e12 / pk["bf16_tflops"]}
+    for name, w in inputs.WORKLOADS.items():
+        if name == main_name or name == "mha_causal_1x256x2x128_f16":  # the oracle-sized case is a parity case
+            continue
+        r = (time_sparse if w.kind == "sparse" else time_dense)(w, steps, warmup, device)
+        d, _ = describe(w, r, pk, pk_kind)
+        out[name] = d
         del r
         torch.cuda.empty_cache()
     return out
