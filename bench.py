@@ -405,6 +405,25 @@ def dist_setup(n):
     return world, rank, local
 
 
+def reduce_max_over_ranks(vals, device=None):
+    """Each value's maximum over all ranks: one all-reduce, outside the timed
+    region.  With one process (or no process group) the values come back as is."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (weak scaling: each rank runs its own copy of the workload)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def run_reference(args):
     """CPU oracle arm: each step times the oracle on a bounded sample."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -447,8 +466,8 @@ def describe(w, r, pk, pk_kind, world=1):
         kname = f"sparse_bwd_kernel<{w.dtype}>"
         t_tensor = flops / (float(pk["bf16_tflops"]) * 1e12)
         t_hbm = by["main"] / (float(pk["hbm_gbs"]) * 1e9)
-        out = {"value": step_bytes * world / (ms * 1e-3) / 1e9, "unit": "GB/s",
-               "TFLOP/s": flops * world / (ms * 1e-3) / 1e12,
+        out = {"value": job_rate(step_bytes, world, ms) / 1e9, "unit": "GB/s",
+               "TFLOP/s": job_rate(flops, world, ms) / 1e12,
                "valid_pairs": sparse_valid_pairs(w, idx), "algorithmic_bytes": by}
         achieved_t = flops / (ms_main * 1e-3) / 1e12
         achieved_b = by["main"] / (ms_main * 1e-3) / 1e9
@@ -462,7 +481,7 @@ def describe(w, r, pk, pk_kind, world=1):
         src = _os.path.join(csrc, "sparse_bwd.cu")
     else:
         flops = dense_flops(w)
-        out = {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s"}
+        out = {"value": job_rate(flops, world, ms) / 1e12, "unit": "TFLOP/s"}
         achieved = flops / (ms_main * 1e-3) / 1e12
         peak = float(pk["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
@@ -526,12 +545,7 @@ def main():
     clocks.start()
     r = timer(w, args.steps, args.warmup, device, world)
     clk = clocks.stop()
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([r["ms_step"], r["ms_main"]], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        r["ms_step"], r["ms_main"] = float(t[0]), float(t[1])
+    r["ms_step"], r["ms_main"] = reduce_max_over_ranks([r["ms_step"], r["ms_main"]], device)
     d, flops = describe(w, r, pk, pk_kind, world)
     line = {
         "metric": METRIC, "value": d["value"], "unit": d["unit"], "n_gpus": world, "steps": args.steps,
