@@ -1,0 +1,585 @@
+// Launch 2 of the dense backward for head dim 128: the persistent,
+// key-block-owned main kernel with 128-query steps.
+//
+// Same placement as the head-dim-64 kernel (the "Tiled" program of the TileOPs
+// MHA backward page, section "TileFoundry Description"; KV-head ownership as in
+// the flash-linear-attention issue "Evaluate KV-head-owned GQA dKV backward",
+// "Bounded scope" items 1-2): a tile is 128 key rows of one KV head, K and V
+// stay in shared memory, dK and dV accumulate in tensor memory over every
+// query block of every query head of the group and are written once.  Per
+// step (BN = 128 queries of one query head):
+//
+//   S^T  = K Q^T        M = 128 keys, N = 128 queries, K = 128   (shared x shared)
+//   dP^T = V dO^T       same shape
+//   P^T  = exp2(S^T*scale*log2e - LSE2), masked; dS^T = P^T o (dP^T - delta)
+//   dV  += P^T dO       A = P^T from TMEM (16-bit pairs), B = dO   N = 128
+//   dK  += dS^T Q       A = dS^T from TMEM                        N = 128
+//   dQ   = dS K         A = dS from shared memory, M = 128 queries, N = 128
+//
+// Every MMA has N = 128.  An M = 128, N = 64 MMA with both operands in shared
+// memory reads 6 KB per 32 cycles of tensor work, more than the 128 bytes
+// per clock shared memory delivers; at N = 128 the operand bytes per flop
+// drop by a quarter and the tensor pipe can run at full rate.
+//
+// Tensor memory (512 columns): S^T [128 x 128] f32 at 0, overwritten by P^T
+// (16-bit pairs, columns 0-63) and dS^T (columns 64-127); dP^T at 128, which
+// the f32 dQ of the step overwrites once the softmax warps have read dP; dV at
+// 256, dK at 384.
+//
+// Shared memory: K, V (32 KB each), two Q/dO stages (64 KB each), the dS tile
+// (32 KB).  The f32 dQ of a step (64 KB) is staged in that step's own Q/dO
+// stage once dV and dK have read it, added into the workspace accumulator with
+// four TMA bulk tensor reduce-adds, and the stage is handed back to the
+// producer after the reduce has read it.
+//
+// Warp roles (14 warps): 0-3 dQ epilogue (lane = query), 4-11 two warpgroups
+// of softmax/dS work (each owns 64 of the 128 query columns of all 128 key
+// rows) that also land dK/dV, 12 TMA producer, 13 MMA issuer.  A stage, a
+// TMEM region or the dS tile is reused only after an mbarrier shows that its
+// last reader is done.  Every wait is bounded.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "cvt.cuh"
+#include "dense_common.cuh"
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace ab {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int BM = kDenseBM;
+constexpr int BN = 128;
+constexpr int ST = 2;                 // Q/dO stages
+constexpr int PREFETCH = 4;           // L2 prefetch distance of Q/dO/LSE/delta, in steps
+constexpr int SLAB = 128 * 128;       // [128 rows x 64 cols] 16-bit, 128-byte swizzled
+constexpr int KV_TILE = 2 * SLAB;     // 128 rows x 128 cols
+constexpr int Q_TILE = 2 * SLAB;
+constexpr int STAGE = 2 * Q_TILE;     // Q then dO
+constexpr int DS_BLOCK = BM * 128;    // dS as [128 keys x 64 queries] 16-bit
+constexpr int STG_SLAB = BN * 128;    // f32 dQ staging: [128 queries x 32 d] per slab, 4 slabs
+
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + KV_TILE;
+constexpr int OFF_STAGE = OFF_V + KV_TILE;
+constexpr int OFF_DS = OFF_STAGE + ST * STAGE;
+constexpr int OFF_LSE = OFF_DS + 2 * DS_BLOCK;
+constexpr int OFF_DELTA = OFF_LSE + ST * BN * 4;
+constexpr int OFF_RING = OFF_DELTA + ST * BN * 4;
+constexpr int OFF_BAR = OFF_RING + 64;
+constexpr int NBAR = 32;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int SMEM = OFF_MISC + 64;
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+static_assert(4 * STG_SLAB == STAGE, "the f32 dQ staging fills one stage");
+static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+constexpr int T_S = 0;     // S^T f32; P^T pairs at 0-63, dS^T pairs at 64-127
+constexpr int T_DP = 128;  // dP^T f32, then the step's dQ f32 [128 queries x 128 d]
+constexpr int T_DV = 256;
+constexpr int T_DK = 384;
+constexpr int THREADS = 14 * 32;
+
+enum Bar : int {
+  FULL0 = 0,        // ST stages: producer's expect_tx arrival + its LSE/delta arrival
+  EMPTY0 = 2,       // ST stages: the dQ reduce has read the staging in the stage
+  KV_FULL = 4,
+  KV_FREE,
+  TILE_FULL0,       // 2 slots
+  TILE_EMPTY0 = 8,  // 2 slots
+  S_FULL = 10,
+  S_FREE,           // dV and dK of the step completed: S^T columns reusable
+  SREAD,            // 8 softmax warps finished reading S^T
+  P_READY,          // 8 softmax warps stored P^T
+  DP_FULL,
+  DS_READY,         // 8 softmax warps stored dS^T (TMEM) and dS (shared)
+  DS_SFREE,         // dQ MMAs read the shared dS tile
+  DQ_FULL,
+  DQ_EMPTY,         // 4 epilogue warps loaded dQ: the dP^T columns are free
+  STG_FULL0,        // ST stages: 4 epilogue warps wrote their staging rows
+  DKV_FULL = STG_FULL0 + ST,
+  DKV_FREE,
+  DRAIN,
+  NUM_BARS
+};
+static_assert(NUM_BARS <= NBAR, "barrier storage");
+
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_constant__ DenseMaps maps,
+                                                                  const DenseParams p) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  TileInfo* ring = reinterpret_cast<TileInfo*>(sm + OFF_RING);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 8);
+  float* s_lse = reinterpret_cast<float*>(sm + OFF_LSE);
+  float* s_delta = reinterpret_cast<float*>(sm + OFF_DELTA);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if ((smem_u32(sm) & 1023u) != 0) {  // the swizzled tiles need an aligned base
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrAlign);
+    return;
+  }
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&bars[FULL0 + i], 2);
+      mbar_init(&bars[EMPTY0 + i], 1);
+      mbar_init(&bars[STG_FULL0 + i], 4);
+    }
+    mbar_init(&bars[KV_FULL], 1);
+    mbar_init(&bars[KV_FREE], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[TILE_FULL0 + i], 1);
+      mbar_init(&bars[TILE_EMPTY0 + i], 13);  // MMA warp + 8 softmax warps + 4 epilogue warps
+    }
+    mbar_init(&bars[S_FULL], 1);
+    mbar_init(&bars[S_FREE], 1);
+    mbar_init(&bars[SREAD], 8);
+    mbar_init(&bars[P_READY], 8);
+    mbar_init(&bars[DP_FULL], 1);
+    mbar_init(&bars[DS_READY], 8);
+    mbar_init(&bars[DS_SFREE], 1);
+    mbar_init(&bars[DQ_FULL], 1);
+    mbar_init(&bars[DQ_EMPTY], 4);
+    mbar_init(&bars[DKV_FULL], 1);
+    mbar_init(&bars[DKV_FREE], 8);
+    mbar_init(&bars[DRAIN], 1);
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 12) {
+    // ============================================================ producer
+    int pend_full[ST];
+#pragma unroll
+    for (int i = 0; i < ST; ++i) pend_full[i] = -1;
+    int kv_pend = -1;
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (tc >= 2 && !(ok = mbar_wait_warp(&bars[TILE_EMPTY0 + slot], ((tc >> 1) - 1) & 1, wc, kErrWaitTile))) break;
+      int t = 0;
+      if (lane == 0) t = atomicAdd(p.tile_counter, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      const TileInfo ti = decode_tile(t, p);
+      if (lane == 0) {
+        ring[slot] = ti;
+        mbar_arrive(&bars[TILE_FULL0 + slot]);
+      }
+      if (!ti.valid) break;
+      if (tc >= 1 && !(ok = mbar_wait_warp(&bars[KV_FREE], (tc - 1) & 1, wc, kErrWaitKVFree))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[KV_FULL], 2 * KV_TILE);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          tma_load_4d(sm + OFF_K + s * SLAB, &maps.k, &bars[KV_FULL], s * 64, ti.g, ti.seq_start + ti.k0, ti.b);
+          tma_load_4d(sm + OFF_V + s * SLAB, &maps.v, &bars[KV_FULL], s * 64, ti.g, ti.seq_start + ti.k0, ti.b);
+        }
+      }
+      kv_pend = tc & 1;
+      const int n = p.G * ti.nq;
+      // LSE2 / delta of a step are loaded into registers one step ahead
+      constexpr int PER_LANE = BN / 32;
+      float nl[PER_LANE], nd[PER_LANE];
+      auto load_rows = [&](int jj) {
+        const int hh = ti.g * p.G + jj / ti.nq, qq = (ti.qlo + jj % ti.nq) * BN;
+        const int64_t rb = (static_cast<int64_t>(ti.b) * p.HQ + hh) * p.S + ti.seq_start;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+          const int q = qq + lane + 32 * i;
+          nl[i] = q < ti.len ? p.lse2[rb + q] : 0.f;
+          nd[i] = q < ti.len ? p.delta[rb + q] : 0.f;
+        }
+      };
+      if (n > 0) load_rows(0);
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
+        const uint32_t r = gs / ST;
+        if (gs >= static_cast<uint32_t>(ST) &&
+            !(ok = mbar_wait_warp(&bars[EMPTY0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
+          break;
+        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
+        uint8_t* sq = sm + OFF_STAGE + st * STAGE;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[FULL0 + st], STAGE);
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            tma_load_4d(sq + s * SLAB, &maps.q, &bars[FULL0 + st], s * 64, h, ti.seq_start + q0, ti.b);
+            tma_load_4d(sq + Q_TILE + s * SLAB, &maps.dO, &bars[FULL0 + st], s * 64, h, ti.seq_start + q0, ti.b);
+          }
+        }
+        // warm L2 with the operands of a step PREFETCH steps ahead
+        if (j + PREFETCH < n) {
+          const int hf = ti.g * p.G + (j + PREFETCH) / ti.nq, qf = (ti.qlo + (j + PREFETCH) % ti.nq) * BN;
+          if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              tma_prefetch_l2_4d(&maps.q, s * 64, hf, ti.seq_start + qf, ti.b);
+              tma_prefetch_l2_4d(&maps.dO, s * 64, hf, ti.seq_start + qf, ti.b);
+            }
+          }
+          const int64_t rf = (static_cast<int64_t>(ti.b) * p.HQ + hf) * p.S + ti.seq_start + qf;
+          if (lane < BN / 32 && qf + lane * 32 < ti.len) {
+            prefetch_l2(p.lse2 + rf + lane * 32);
+            prefetch_l2(p.delta + rf + lane * 32);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+          s_lse[st * BN + lane + 32 * i] = nl[i];
+          s_delta[st * BN + lane + 32 * i] = nd[i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[FULL0 + st]);
+        if (j + 1 < n) load_rows(j + 1);
+        pend_full[st] = r & 1;
+      }
+    }
+    // loads still in flight land before the CTA exits
+    if (lane == 0) {
+      if (kv_pend >= 0) mbar_drain(&bars[KV_FULL], kv_pend);
+#pragma unroll
+      for (int i = 0; i < ST; ++i)
+        if (pend_full[i] >= 0) mbar_drain(&bars[FULL0 + i], pend_full[i]);
+    }
+  } else if (warp == 13) {
+    // ============================================================ MMA issuer (whole warp, one elected lane)
+    constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, BN, false, false);
+    constexpr uint32_t IDESC_KV = idesc_f16(BF16, 128, D, false, true);
+    constexpr uint32_t IDESC_DQ = idesc_f16(BF16, 128, D, true, true);
+    const uint32_t sbase = smem_u32(sm);
+    // K-major K-steps add 32 bytes inside a 128-byte row (slab kk/4); MN-major
+    // K-steps add 16 rows = 2048 bytes
+    const uint64_t dK_kmaj = sdesc_sw128(sbase + OFF_K, 16, 1024);
+    const uint64_t dV_kmaj = sdesc_sw128(sbase + OFF_V, 16, 1024);
+    const uint64_t dQ_kmaj = sdesc_sw128(sbase + OFF_STAGE, 16, 1024);
+    const uint64_t dO_kmaj = sdesc_sw128(sbase + OFF_STAGE + Q_TILE, 16, 1024);
+    const uint64_t dQ_mn = sdesc_sw128(sbase + OFF_STAGE, SLAB, 1024);
+    const uint64_t dO_mn = sdesc_sw128(sbase + OFF_STAGE + Q_TILE, SLAB, 1024);
+    const uint64_t dK_mn = sdesc_sw128(sbase + OFF_K, SLAB, 1024);
+    const uint64_t dDS_mn = sdesc_sw128(sbase + OFF_DS, DS_BLOCK, 1024);
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+      const TileInfo ti = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+      if (!ti.valid) break;
+      const int n = p.G * ti.nq;
+      if (!(ok = mbar_wait_warp(&bars[KV_FULL], tc & 1, wc, kErrWaitKV))) break;
+      tc_fence_after();
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
+        const uint64_t so = sdesc_step(st * STAGE);
+        // ---- S^T: the stage is loaded and dV/dK of the previous step have read P^T/dS^T
+        if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
+        if (gs >= 1 && !(ok = mbar_wait_warp(&bars[S_FREE], (gs - 1) & 1, wc, kErrWaitSFree))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ko = sdesc_step((kk / 4) * SLAB + (kk % 4) * 32);
+          mma_ss_w(tmem + T_S, dK_kmaj + ko, dQ_kmaj + so + ko, IDESC_S, kk > 0);
+        }
+        mma_commit_w(&bars[S_FULL]);
+        // ---- dP^T: the epilogue has loaded the previous step's dQ from these columns
+        if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DQ_EMPTY], (gs - 1) & 1, wc, kErrWaitDQEmpty))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ko = sdesc_step((kk / 4) * SLAB + (kk % 4) * 32);
+          mma_ss_w(tmem + T_DP, dV_kmaj + ko, dO_kmaj + so + ko, IDESC_S, kk > 0);
+        }
+        mma_commit_w(&bars[DP_FULL]);
+        // ---- dV += P^T dO (A = P^T pairs, 8 columns per 16 queries; B = dO MN-major)
+        if (!(ok = mbar_wait_warp(&bars[P_READY], gs & 1, wc, kErrWaitP))) break;
+        if (j == 0 && tc >= 1 && !(ok = mbar_wait_warp(&bars[DKV_FREE], (tc - 1) & 1, wc, kErrWaitDKVFree))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_w(tmem + T_DV, tmem + T_S + kk * 8, dO_mn + so + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
+        // ---- dK += dS^T Q
+        if (!(ok = mbar_wait_warp(&bars[DS_READY], gs & 1, wc, kErrWaitDS))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_w(tmem + T_DK, tmem + T_S + BN / 2 + kk * 8, dQ_mn + so + sdesc_step(kk * 2048), IDESC_KV,
+                   j > 0 || kk > 0);
+        mma_commit_w(&bars[S_FREE]);
+        // ---- dQ = dS K over the 128 key rows (A = dS MN-major in two 64-query blocks, B = K MN-major),
+        // into the dP^T columns (the softmax warps read dP before publishing dS)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ss_w(tmem + T_DP, dDS_mn + sdesc_step(kk * 2048), dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
+        mma_commit_w(&bars[DQ_FULL]);
+        mma_commit_w(&bars[DS_SFREE]);
+      }
+      if (!ok) break;
+      if (n == 0 && tc >= 1 && !(ok = mbar_wait_warp(&bars[DKV_FREE], (tc - 1) & 1, wc, kErrWaitDKVFree))) break;
+      mma_commit_w(&bars[KV_FREE]);   // last readers of K and V issued
+      mma_commit_w(&bars[DKV_FULL]);  // dK, dV final once every MMA of the tile completed
+    }
+    // every MMA issued by this warp completes before TMEM is released
+    mma_commit_w(&bars[DRAIN]);
+    if (lane == 0) mbar_drain(&bars[DRAIN], 0);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============================================================ softmax / dS, dK / dV landing
+    const int wg = (warp - 4) >> 2, quad = warp & 3;
+    const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    constexpr int HALF = BN / 2;  // query columns of this warpgroup
+    constexpr int NCH = HALF / 32;
+    const bool cm = p.causal || p.window > 0;
+    const int W = p.window;
+    float pv[HALF];
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+      const TileInfo ti = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+      if (!ti.valid) break;
+      const int n = p.G * ti.nq;
+      const int kpos = ti.k0 + row;
+      const bool kvalid = kpos < ti.len;
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
+        const uint32_t sb = tmem + lane_off + T_S;
+        const int q0 = (ti.qlo + j % ti.nq) * BN;
+        const int qc0 = q0 + wg * HALF;  // first (sequence-local) query of my columns
+        // fully visible block: every key and query in range and inside the mask
+        const bool full_vis = ti.k0 + BM <= ti.len && q0 + BN <= ti.len && (!cm || q0 >= ti.k0 + BM - 1) &&
+                              (W <= 0 || q0 + BN - 1 < ti.k0 + W);
+        const float4* lse4 = reinterpret_cast<const float4*>(s_lse + st * BN + wg * HALF);
+        const float4* dlt4 = reinterpret_cast<const float4*>(s_delta + st * BN + wg * HALF);
+        if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
+        if (!(ok = mbar_wait_warp(&bars[S_FULL], gs & 1, wc, kErrWaitS))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(sb + wg * HALF + ch * 32, r);
+          float lse[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 t = lse4[ch * 8 + c4];
+            lse[4 * c4] = t.x, lse[4 * c4 + 1] = t.y, lse[4 * c4 + 2] = t.z, lse[4 * c4 + 3] = t.w;
+          }
+          tmem_ld_wait();
+          if (full_vis) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int cc = ch * 32 + c, q = qc0 + cc;
+              bool vis = kvalid && q < ti.len;
+              if (cm) vis = vis && kpos <= q;
+              if (W > 0) vis = vis && q < kpos + W;
+              pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c])) : 0.f;
+            }
+          }
+        }
+        // P^T overwrites S^T columns the other warpgroup reads: all eight
+        // warps finish reading S^T first.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[SREAD]);
+        if (!(ok = mbar_wait_warp(&bars[SREAD], gs & 1, wc, kErrWaitSRead))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
+          tmem_st16(sb + (wg * HALF + ch * 32) / 2, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[P_READY]);
+
+        if (!(ok = mbar_wait_warp(&bars[DP_FULL], gs & 1, wc, kErrWaitDP))) break;
+        // the dS tile this step writes was last read by the previous step's dQ
+        if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DS_SFREE], (gs - 1) & 1, wc, kErrWaitDSFree))) break;
+        tc_fence_after();
+        uint8_t* dsb = sm + OFF_DS + wg * DS_BLOCK;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + T_DP + wg * HALF + ch * 32, r);
+          float dlt[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 t = dlt4[ch * 8 + c4];
+            dlt[4 * c4] = t.x, dlt[4 * c4 + 1] = t.y, dlt[4 * c4 + 2] = t.z, dlt[4 * c4 + 3] = t.w;
+          }
+          tmem_ld_wait();
+          uint32_t dsw[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int cc = ch * 32 + c;
+            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[c]);
+            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[c + 1]);
+            dsw[c / 2] = pack2<BF16>(d0, d1);
+          }
+          // dS^T pairs into columns 64-127 (the S^T there is read), and dS as the
+          // MN-major A operand of dQ: 64-query block wg, row = key, 16-byte chunks 4ch..4ch+3
+          tmem_st16(sb + BN / 2 + (wg * HALF + ch * 32) / 2, dsw);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(dsb + sw128_offset(row, ch * 4 + c4)) =
+                make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[DS_READY]);
+      }
+      if (!ok) break;
+      // ---- dK / dV of the tile: warpgroup 0 lands dV, warpgroup 1 lands dK (times sm_scale)
+      if (!(ok = mbar_wait_warp(&bars[DKV_FULL], tc & 1, wc, kErrWaitDKV))) break;
+      tc_fence_after();
+      const bool isK = wg == 1;
+      const uint32_t col0 = isK ? T_DK : T_DV;
+      const float mul = isK ? p.sm_scale : 1.f;
+      const int64_t pos = ti.seq_start + kpos;
+      uint8_t* out = isK ? p.dk + 2 * (ti.b * p.sdk_b + pos * p.sdk_s + ti.g * p.sdk_h)
+                         : p.dv + 2 * (ti.b * p.sdv_b + pos * p.sdv_s + ti.g * p.sdv_h);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_off + col0 + ch * 32, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
+        if (ch == D / 32 - 1) {  // the accumulators may be overwritten by the next tile from here on
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[DKV_FREE]);
+        }
+        if (kvalid) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 v;
+            v.x = pack2<BF16>(__uint_as_float(r[c8 * 8 + 0]) * mul, __uint_as_float(r[c8 * 8 + 1]) * mul);
+            v.y = pack2<BF16>(__uint_as_float(r[c8 * 8 + 2]) * mul, __uint_as_float(r[c8 * 8 + 3]) * mul);
+            v.z = pack2<BF16>(__uint_as_float(r[c8 * 8 + 4]) * mul, __uint_as_float(r[c8 * 8 + 5]) * mul);
+            v.w = pack2<BF16>(__uint_as_float(r[c8 * 8 + 6]) * mul, __uint_as_float(r[c8 * 8 + 7]) * mul);
+            *reinterpret_cast<uint4*>(out + 2 * (ch * 32 + c8 * 8)) = v;
+          }
+        }
+      }
+    }
+  } else {
+    // ============================================================ dQ epilogue (lane = query)
+    const int quad = warp;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int q = quad * 32 + lane;  // query of the block = TMEM lane
+    const bool leader = warp == 0 && lane == 0;
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int tc = 0; ok; ++tc) {
+      const int slot = tc & 1;
+      if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+      const TileInfo ti = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+      if (!ti.valid) break;
+      const int n = p.G * ti.nq;
+      for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
+        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
+        // dQ complete (so dV and dK, issued before it, have read this step's stage)
+        if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
+        tc_fence_after();
+        // f32 staging in the stage: four 128-byte-swizzled slabs [128 queries x 32 d]
+        uint8_t* stg = sm + OFF_STAGE + st * STAGE;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[64];
+          tmem_ld32(tmem + lane_off + T_DP + 64 * hf, r);
+          tmem_ld32(tmem + lane_off + T_DP + 64 * hf + 32, r + 32);
+          tmem_ld_wait();
+          if (hf == 1) {  // dQ fully loaded: the dP^T columns may be overwritten
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[DQ_EMPTY]);
+          }
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int slab = 2 * hf + (c >> 3), chunk = c & 7;
+            *reinterpret_cast<float4*>(stg + slab * STG_SLAB + sw128_offset(q, chunk)) =
+                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
+                            __uint_as_float(r[4 * c + 3]));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[STG_FULL0 + st]);
+        bool lok = true;
+        if (leader) {
+          lok = mbar_wait(&bars[STG_FULL0 + st], (gs / ST) & 1, wc, kErrWaitStage);
+          if (lok) {
+            const int c2 = ti.seq_start + q0;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
+            bulk_commit_group();
+            bulk_wait_read_all();  // the stage may be reloaded once the reduce has read it
+            mbar_arrive(&bars[EMPTY0 + st]);
+          }
+        }
+        if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
+      }
+    }
+    if (leader) bulk_wait_all();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_t(const DenseParams& p, const DenseMaps& m, int grid, cudaStream_t st) {
+  auto kern = dense128_bwd_kernel<BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, THREADS, SMEM, st>>>(m, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dense128(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st) {
+  return bf16 ? launch_t<true>(p, m, grid, st) : launch_t<false>(p, m, grid, st);
+}
+
+}  // namespace ab

@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "cvt.cuh"
+#include "dense_common.cuh"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -117,49 +118,6 @@ enum Bar : int {
   NUM_BARS
 };
 static_assert(NUM_BARS <= 32, "barrier storage");
-
-struct TileInfo {
-  int b, g, seq_start, len, k0, qlo, nq, valid;
-};
-
-// Tile t -> (batch, KV head, key block); longest tiles first (smallest key
-// block index first, which is the longest under a causal mask).
-__device__ TileInfo decode_tile(int t, const DenseParams& p) {
-  TileInfo ti{};
-  ti.valid = 0;
-  const int BH = p.B * p.HKV;
-  if (t < 0) return ti;
-  const int bh = t % BH;
-  int r = t / BH;
-  ti.b = bh / p.HKV;
-  ti.g = bh % p.HKV;
-  if (p.cu_seqlens != nullptr) {
-    bool found = false;
-    for (int n = 0; n < p.num_seqs; ++n) {
-      const int a = clamp_pos(p.cu_seqlens[n], p.S), e = clamp_pos(p.cu_seqlens[n + 1], p.S);
-      const int nt = e > a ? (e - a + kDenseBM - 1) / kDenseBM : 0;
-      if (r < nt) {
-        ti.seq_start = a;
-        ti.len = e - a;
-        found = true;
-        break;
-      }
-      r -= nt;
-    }
-    if (!found) return ti;
-  } else {
-    if (static_cast<int64_t>(r) * kDenseBM >= p.S) return ti;
-    ti.seq_start = 0;
-    ti.len = p.S;
-  }
-  ti.k0 = r * kDenseBM;
-  int lo, hi;
-  query_block_range(ti.k0, kDenseBM, ti.len, p.causal, p.window, dense_bn(p.D), &lo, &hi);
-  ti.qlo = lo;
-  ti.nq = hi - lo;
-  ti.valid = 1;
-  return ti;
-}
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
@@ -746,6 +704,8 @@ __global__ void selftest_timeout_kernel(int* err, uint64_t timeout_ns) {
 }  // namespace
 
 cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st) {
+  if (p.D == 128 && p.bn == 128) return launch_dense128(p, m, bf16, grid, st);
+  if (p.bn != dense_bn(p.D)) return cudaErrorInvalidValue;
   if (p.D == 128) return bf16 ? launch_dense_t<128, true>(p, m, grid, st) : launch_dense_t<128, false>(p, m, grid, st);
   return bf16 ? launch_dense_t<64, true>(p, m, grid, st) : launch_dense_t<64, false>(p, m, grid, st);
 }

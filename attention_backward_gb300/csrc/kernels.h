@@ -50,6 +50,7 @@ struct DenseParams {
   int64_t sdv_b, sdv_s, sdv_h;
   uint64_t timeout_ns;
   int* tile_counter;  // zeroed by the preprocess; persistent CTAs draw tiles from it
+  int bn;             // query rows per step (the tile schedule's query block)
 };
 
 struct DenseMaps {
@@ -84,10 +85,19 @@ cudaError_t launch_sparse(const SparseParams& p, const SparseMaps& m, bool bf16,
 cudaError_t launch_preprocess(const PreprocessParams& p, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_land(const LandParams& p, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);
+// Head dim 128 with 128-query steps (dense128_bwd.cu); launch_dense forwards
+// launches with p.bn == 128 and p.D == 128 here.
+cudaError_t launch_dense128(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_selftest_timeout(int* err, uint64_t timeout_ns, cudaStream_t st);
 
 // Block sizes of the dense kernel (keys per tile, queries per step).
 constexpr int kDenseBM = 128;
+// Query rows per step of the key-block kernel of dense_bwd.cu (64 for head dim
+// 128, whose double-buffered S^T then fits tensor memory; 128 for head dim 64).
 __host__ __device__ constexpr int dense_bn(int D) { return D == 128 ? 64 : 128; }
+// Query rows per step of a dense launch: head dim 128 without a causal or
+// window mask (long key tiles) runs the 128-query kernel of dense128_bwd.cu,
+// every other launch the kernel of dense_bwd.cu.
+inline int dense_launch_bn(int D, bool masked) { return D == 128 && !masked ? 128 : dense_bn(D); }
 
 }  // namespace ab

@@ -42,6 +42,10 @@ SMALL = [
                   dtype="f16"),
     inputs.scaled(C4, name="varlen_d128_w300", D=128, Dv=128, S=900, HQ=4, HKV=2, window=300,
                   cu_seqlens=(0, 400, 900)),
+    # head dim 128 without a mask runs the 128-query-step kernel: packed sequences
+    # with a ragged last block
+    inputs.scaled(C4, name="varlen_d128_noncausal", D=128, Dv=128, S=420, HQ=4, HKV=2, causal=False, window=-1,
+                  cu_seqlens=(0, 150, 420)),
 ]
 
 
