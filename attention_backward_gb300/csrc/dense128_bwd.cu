@@ -377,24 +377,30 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
           tmem_ld32(sb + wg * HALF + ch * 32, r);
-          float lse[32];
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 t = lse4[ch * 8 + c4];
-            lse[4 * c4] = t.x, lse[4 * c4 + 1] = t.y, lse[4 * c4 + 2] = t.z, lse[4 * c4 + 3] = t.w;
-          }
           tmem_ld_wait();
+          // LSE2 four columns at a time, so that only r and pv stay live
           if (full_vis) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c]));
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 t = lse4[ch * 8 + c4];
+              const float l4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                pv[ch * 32 + 4 * c4 + e] = ex2(fmaf(__uint_as_float(r[4 * c4 + e]), p.scale_log2, -l4[e]));
+            }
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int cc = ch * 32 + c, q = qc0 + cc;
-              bool vis = kvalid && q < ti.len;
-              if (cm) vis = vis && kpos <= q;
-              if (W > 0) vis = vis && q < kpos + W;
-              pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c])) : 0.f;
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 t = lse4[ch * 8 + c4];
+              const float l4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * c4 + e, cc = ch * 32 + c, q = qc0 + cc;
+                bool vis = kvalid && q < ti.len;
+                if (cm) vis = vis && kpos <= q;
+                if (W > 0) vis = vis && q < kpos + W;
+                pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -l4[e])) : 0.f;
+              }
             }
           }
         }
@@ -426,19 +432,14 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + T_DP + wg * HALF + ch * 32, r);
-          float dlt[32];
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 t = dlt4[ch * 8 + c4];
-            dlt[4 * c4] = t.x, dlt[4 * c4 + 1] = t.y, dlt[4 * c4 + 2] = t.z, dlt[4 * c4 + 3] = t.w;
-          }
           tmem_ld_wait();
           uint32_t dsw[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const int cc = ch * 32 + c;
-            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[c]);
-            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[c + 1]);
+            const float2 dl = reinterpret_cast<const float2*>(dlt4)[cc / 2];  // delta of columns cc, cc + 1
+            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dl.x);
+            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dl.y);
             dsw[c / 2] = pack2<BF16>(d0, d1);
           }
           // dS^T pairs into columns 64-127 (the S^T there is read), and dS as the
