@@ -485,8 +485,10 @@ def describe(w, r, pk, pk_kind, world=1):
         achieved = flops / (ms_main * 1e-3) / 1e12
         peak = float(pk["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
-        kname = f"dense_bwd_kernel<{w.D},{w.dtype}>"
-        src = _os.path.join(csrc, "dense_bwd.cu")
+        if w.D == 128 and not (w.causal or w.window > 0):  # unmasked head dim 128: 128-query steps
+            kname, src = f"dense128_bwd_kernel<{w.dtype}>", _os.path.join(csrc, "dense128_bwd.cu")
+        else:
+            kname, src = f"dense_bwd_kernel<{w.D},{w.dtype}>", _os.path.join(csrc, "dense_bwd.cu")
     roof["traffic"] = traffic_record(src, kname + "@" + w.name)
     roof["peak_kind"] = f"{'bf16 burst' if roof['bound'] == 'tensor' else 'copy'}, {pk_kind}"
     roof["kernel"] = kname
