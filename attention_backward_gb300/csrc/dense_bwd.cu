@@ -319,11 +319,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             // the buffer's previous readers: dV/dK of step nxt-2 (D = 128), or the
             // epilogue's readout of the dQ that overwrote it (D = 64; readouts are
             // in step order, so the latest issued dQ is waited for)
-            const bool ok2 = D == 128
-                                 ? mbar_wait_warp(&bars[S_FREE0 + (nxt & 1)], ((nxt - 2) >> 1) & 1, wc, kErrWaitSFree)
-                                 : mbar_wait_warp(&bars[DQ_EMPTY], static_cast<uint32_t>(last_dq) & 1, wc,
-                                                  kErrWaitDQEmpty);
-            if (!(ok = ok2)) break;
+            ok = D == 128 ? mbar_wait_warp(&bars[S_FREE0 + (nxt & 1)], ((nxt - 2) >> 1) & 1, wc, kErrWaitSFree)
+                          : mbar_wait_warp(&bars[DQ_EMPTY], static_cast<uint32_t>(last_dq) & 1, wc, kErrWaitDQEmpty);
+            if (!ok) break;
           }
           tc_fence_after();
           const uint32_t dS_acc = tmem + C::T_SB + (nxt & 1) * BN;
@@ -427,7 +425,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     const bool cm = p.causal || p.window > 0;
     const int W = p.window;
     float pv[HALF];
-    uint32_t dsw[HALF / 2];
     uint32_t gs = 0;
     bool ok = true;
     for (int tc = 0; ok; ++tc) {
@@ -457,25 +454,55 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
           tmem_ld32(sb + wg * HALF + ch * 32, r);
-          float lse[32];
+          if constexpr (NCH == 1) {
+            // one chunk per thread: LSE2 is read while the TMEM load is in flight
+            float lse[32];
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 t = lse4[ch * 8 + c4];
-            lse[4 * c4] = t.x, lse[4 * c4 + 1] = t.y, lse[4 * c4 + 2] = t.z, lse[4 * c4 + 3] = t.w;
-          }
-          tmem_ld_wait();
-          if (full_vis) {
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 t = lse4[ch * 8 + c4];
+              lse[4 * c4] = t.x, lse[4 * c4 + 1] = t.y, lse[4 * c4 + 2] = t.z, lse[4 * c4 + 3] = t.w;
+            }
+            tmem_ld_wait();
+            if (full_vis) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c]));
+              for (int c = 0; c < 32; ++c)
+                pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int cc = ch * 32 + c, q = qc0 + cc;
+                bool vis = kvalid && q < ti.len;
+                if (cm) vis = vis && kpos <= q;
+                if (W > 0) vis = vis && q < kpos + W;
+                pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c])) : 0.f;
+              }
+            }
           } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int cc = ch * 32 + c, q = qc0 + cc;
-              bool vis = kvalid && q < ti.len;
-              if (cm) vis = vis && kpos <= q;
-              if (W > 0) vis = vis && q < kpos + W;
-              pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c])) : 0.f;
+            tmem_ld_wait();
+            // LSE2 four columns at a time, so that only r and pv stay live
+            if (full_vis) {
+  #pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 t = lse4[ch * 8 + c4];
+                const float l4[4] = {t.x, t.y, t.z, t.w};
+  #pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  pv[ch * 32 + 4 * c4 + e] = ex2(fmaf(__uint_as_float(r[4 * c4 + e]), p.scale_log2, -l4[e]));
+              }
+            } else {
+  #pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 t = lse4[ch * 8 + c4];
+                const float l4[4] = {t.x, t.y, t.z, t.w};
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c = 4 * c4 + e, cc = ch * 32 + c, q = qc0 + cc;
+                  bool vis = kvalid && q < ti.len;
+                  if (cm) vis = vis && kpos <= q;
+                  if (W > 0) vis = vis && q < kpos + W;
+                  pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -l4[e])) : 0.f;
+                }
+              }
             }
           }
         }
@@ -499,7 +526,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         if (lane == 0) mbar_arrive(&bars[P_READY0 + (gs & 1)]);
 
         if (!(ok = mbar_wait_warp(&bars[DP_FULL], gs & 1, wc, kErrWaitDP))) break;
+        // the dS tile this step writes was last read by the dQ of step gs - NDS
+        auto ds_tile_free = [&]() -> bool {
+          return gs < static_cast<uint32_t>(C::NDS) ||
+                 mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree);
+        };
+        if (NCH > 1 && !(ok = ds_tile_free())) break;
         tc_fence_after();
+        // each 32-query chunk of dS is stored as soon as it is computed, so only
+        // one chunk of packed pairs is live next to P
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
@@ -516,38 +551,38 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[DP_FREE]);
           }
+          uint32_t dsw[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const int cc = ch * 32 + c;
             const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[c]);
             const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[c + 1]);
-            dsw[cc / 2] = pack2<BF16>(d0, d1);
+            dsw[c / 2] = pack2<BF16>(d0, d1);
+          }
+          if (NCH == 1) {
+            if (!(ok = ds_tile_free())) break;
+            tc_fence_after();
+          }
+          // dS^T into the second half of this step's S^T buffer (its S^T is read)
+          tmem_st16(sb + BN / 2 + (wg * HALF + ch * 32) / 2, dsw);
+          if constexpr (D == 128) {
+            // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
+            // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``
+            uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              *reinterpret_cast<uint4*>(base + sw128_offset(row, wg * 4 + c4)) =
+                  make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+          } else {
+            // dS as the MN-major A operand: 64-query block wg, row = key, chunks 4ch .. 4ch+3
+            uint8_t* base = sm + C::OFF_DS + wg * (BM * 128);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              *reinterpret_cast<uint4*>(base + sw128_offset(row, ch * 4 + c4)) =
+                  make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
           }
         }
-        // the dS tile this step writes was last read by the dQ of step gs - NDS
-        if (gs >= static_cast<uint32_t>(C::NDS) &&
-            !(ok = mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree)))
-          break;
-        tc_fence_after();
-        // dS^T into the second half of this step's S^T buffer (its S^T is read)
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) tmem_st16(sb + BN / 2 + (wg * HALF + ch * 32) / 2, dsw + ch * 16);
-        if constexpr (D == 128) {
-          // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
-          // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``
-          uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES;
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            *reinterpret_cast<uint4*>(base + sw128_offset(row, wg * 4 + c4)) =
-                make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
-        } else {
-          // dS as the MN-major A operand: 64-query block wg, row = key
-          uint8_t* base = sm + C::OFF_DS + wg * (BM * 128);
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<uint4*>(base + sw128_offset(row, c8)) =
-                make_uint4(dsw[c8 * 4], dsw[c8 * 4 + 1], dsw[c8 * 4 + 2], dsw[c8 * 4 + 3]);
-        }
+        if (!ok) break;
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
