@@ -171,8 +171,10 @@ attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* 
   p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.Dv = static_cast<int>(Dv);
   p.lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
   p.delta = reinterpret_cast<float*>(ws + L.delta_off);
-  p.zero = reinterpret_cast<float4*>(ws + L.dq_off);
-  p.zero_n4 = (L.total - L.dq_off) / 16;
+  p.dq_zero = reinterpret_cast<float4*>(ws + L.dq_off);
+  p.dq_row_n4 = static_cast<int>(Dq / 4);
+  p.zero = reinterpret_cast<float4*>(ws + L.dkv_off);
+  p.zero_n4 = (L.total - L.dkv_off) / 16;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   return launch_status(launch_preprocess(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
 }

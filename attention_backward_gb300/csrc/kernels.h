@@ -19,7 +19,9 @@ struct PreprocessParams {
   int B, S, H, Dv;
   float* lse2;   // [B,H,S]
   float* delta;  // [B,H,S]
-  float4* zero;  // accumulators to clear
+  float4* dq_zero;     // f32 dQ accumulator [B,S,H,Dq], cleared row by row with delta
+  int dq_row_n4;       // float4 per accumulator row (Dq / 4; 0 without one)
+  float4* zero;        // other accumulators to clear (the sparse dKV accumulator)
   int64_t zero_n4;
   WsHeader* hdr;
 };

@@ -3,8 +3,9 @@
 // Preprocess: delta_i = sum_d O_id dO_id in f32 (the delta row preprocess of
 // the TileOPs MHA backward page, "delta_rows"), LSE2 = LSE * log2(e) so that
 // the main kernel evaluates P with one FFMA and one exp2, zeroed f32
-// accumulators, cleared workspace header.  HBM-bound: 16-byte loads, grid a
-// multiple of the SM count.
+// accumulators (the dQ accumulator row by row next to the delta of the same
+// row), cleared workspace header.  HBM-bound: 16-byte loads and stores, grid
+// a multiple of the SM count.
 //
 // Landing: out = cast(scale * acc) from an f32 accumulator laid out
 // [B,S,H,D] into a strided 16-bit BSHD tensor (the page's "dq_land").
@@ -65,6 +66,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreprocessParams p) {
       h = r % p.H;
       s = (r / p.H) % p.S;
       b = r / (static_cast<int64_t>(p.H) * p.S);
+      // the row's dQ accumulator (same (b, s, h) order), so that its writes
+      // overlap the O/dO reads
+      float4* z = p.dq_zero + r * p.dq_row_n4;
+      for (int k = lig; k < p.dq_row_n4; k += gs) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       const uint4* o = reinterpret_cast<const uint4*>(p.o + 2 * (b * p.so_b + s * p.so_s + h * p.so_h));
       const uint4* d = reinterpret_cast<const uint4*>(p.dO + 2 * (b * p.sdo_b + s * p.sdo_s + h * p.sdo_h));
       for (int c = lig; c < chunks; c += gs) {
