@@ -277,7 +277,7 @@ attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, 
   if (!q || !kv || !dO || !idx || !dq || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || H % HKV != 0 || topk < 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
-  if (DQK != 576 || DV != 512 || H / HKV != 64) return ATTN_ERR_UNSUPPORTED;
+  if (DQK != 576 || DV != 512 || H / HKV > 64) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
   if (B * S * HKV >= (int64_t(1) << 31) || B * SKV * HKV >= (int64_t(1) << 31) || topk >= (int64_t(1) << 31))
     return ATTN_ERR_UNSUPPORTED;
@@ -300,6 +300,7 @@ attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, 
   SparseParams p{};
   p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.SKV = static_cast<int>(SKV);
   p.H = static_cast<int>(H), p.HKV = static_cast<int>(HKV), p.topk = static_cast<int>(topk);
+  p.gh = static_cast<int>(H / HKV);
   p.sm_scale = sm_scale;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);

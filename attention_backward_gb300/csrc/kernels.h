@@ -62,6 +62,7 @@ struct DenseMaps {
 
 struct SparseParams {
   int B, S, SKV, H, HKV, topk;
+  int gh;            // query heads per KV group (at most 64; a unit pads them to 64)
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
   const float* lse2;   // [B,H,S]

@@ -1,7 +1,9 @@
 // Launch 2 of the top-k sparse backward over shared latent rows (the tilelang
 // pull request "Adaptive threads for sparse MLA backward": H = 64 query heads
 // per KV group, one latent row of DQK = 576 per key with V its first DV = 512
-// columns, top-k index lists).
+// columns, top-k index lists).  Smaller groups (the page's tensor-parallel
+// splits, "Applicability") are padded to 64 heads: the padding heads get an
+// infinite LSE, so their P and dS are exactly zero, at 64/G times the work.
 //
 // A unit of work is one (batch, token t, KV group g) with all 64 of its query
 // heads.  Its index list is processed in blocks of BK = 128 slots; per block:
@@ -186,10 +188,17 @@ __global__ void __maxnreg__(168)
         }
         for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
         nb = last < 0 ? 0 : last / BK + 1;
+        // a group of gh < 64 heads is padded to 64: the padding heads get an
+        // infinite LSE, so their P and dS are exactly 0 and add nothing to dKV
         for (int h = lane; h < SH; h += 32) {
-          const int64_t r = (static_cast<int64_t>(b) * p.H + g * SH + h) * p.S + t;
-          ui->lse2[h] = p.lse2[r];
-          ui->delta[h] = p.delta[r];
+          if (h < p.gh) {
+            const int64_t r = (static_cast<int64_t>(b) * p.H + g * p.gh + h) * p.S + t;
+            ui->lse2[h] = p.lse2[r];
+            ui->delta[h] = p.delta[r];
+          } else {
+            ui->lse2[h] = __int_as_float(0x7f800000);
+            ui->delta[h] = 0.f;
+          }
         }
       }
       if (lane == 0) {
@@ -251,7 +260,7 @@ __global__ void __maxnreg__(168)
               mbar_arrive_expect_tx(&bars[RING_FULL0 + rs], CHUNK);
               const bool isq = (i & 1) == 0;
               const int c = i >> 1;
-              tma_load_4d(sm + OFF_RING + rs * CHUNK, isq ? &maps.q : &maps.dO, &bars[RING_FULL0 + rs], c * 64, g * SH,
+              tma_load_4d(sm + OFF_RING + rs * CHUNK, isq ? &maps.q : &maps.dO, &bars[RING_FULL0 + rs], c * 64, g * p.gh,
                           t, b);
             }
             ring_used |= 1u << rs;
@@ -428,7 +437,7 @@ __global__ void __maxnreg__(168)
       // ---- dQ of the token: tile m, lane = head dim 128m + row, columns = heads
       if (!(ok = mbar_wait_warp(&bars[DQ_DONE], uc & 1, wc, kErrSparseBase + 17))) break;
       tc_fence_after();
-      uint8_t* dq = p.dq + 2 * (b * p.sdq_b + static_cast<int64_t>(t) * p.sdq_s + (static_cast<int64_t>(g) * SH) * p.sdq_h);
+      uint8_t* dq = p.dq + 2 * (b * p.sdq_b + static_cast<int64_t>(t) * p.sdq_s + (static_cast<int64_t>(g) * p.gh) * p.sdq_h);
 #pragma unroll 1
       for (int m = 0; m < 5; ++m) {
         uint32_t r[64];
@@ -444,8 +453,10 @@ __global__ void __maxnreg__(168)
         if (d < DQK) {
 #pragma unroll
           for (int h = 0; h < SH; ++h) {
-            const uint32_t w = pack2<BF16>(__uint_as_float(r[h]), 0.f);
-            *reinterpret_cast<uint16_t*>(dq + 2 * (h * p.sdq_h + d)) = static_cast<uint16_t>(w & 0xffffu);
+            if (h < p.gh) {  // the group's own heads (padding heads are not written)
+              const uint32_t w = pack2<BF16>(__uint_as_float(r[h]), 0.f);
+              *reinterpret_cast<uint16_t*>(dq + 2 * (h * p.sdq_h + d)) = static_cast<uint16_t>(w & 0xffffu);
+            }
           }
         }
       }

@@ -151,7 +151,10 @@ ATTN_BWD_API attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_
  *   q, dq : [B,S,H,DQK];  kv : [B,SKV,HKV,DQK] stored densely (row stride
  *   DQK); dO : [B,S,H,DV] 16-bit
  *   idx : int32 [B,S,HKV,topk] with strides sidx (slot stride 1)
- *   DQK = 576, DV = 512;  H / HKV = 64;  topk >= 1. */
+ *   DQK = 576, DV = 512;  G = H / HKV <= 64;  topk >= 1.  A group of G < 64
+ *   heads (a tensor-parallel split of the heads) is computed padded to 64 heads
+ *   whose extra rows contribute exactly zero, so it takes 64/G times the work
+ *   of its own heads. */
 ATTN_BWD_API attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
                                            const void* dO, attn_strides_t sdo, const int32_t* idx,
                                            attn_strides_t sidx, int64_t B, int64_t S, int64_t SKV, int64_t H,

@@ -16,6 +16,12 @@ SMALL = [
     inputs.scaled(C5, name="s300_topk128", S=300, topk=128),
     inputs.scaled(C5, name="s260_topk200_f16", S=260, topk=200, dtype="f16"),
     inputs.scaled(C5, name="s150_topk256_hkv2_b2", B=2, S=150, HQ=128, HKV=2, topk=256),
+    # groups smaller than 64 heads (tensor-parallel splits), computed padded to 64:
+    # padding past the last head (zero-filled), padding taken from the next group's
+    # heads, and a group size that is not a power of two
+    inputs.scaled(C5, name="s200_h32_topk128", S=200, HQ=32, HKV=1, topk=128),
+    inputs.scaled(C5, name="s180_h64_hkv4_topk96_f16", S=180, HQ=64, HKV=4, topk=96, dtype="f16"),
+    inputs.scaled(C5, name="s160_h48_hkv2_topk130", S=160, HQ=48, HKV=2, topk=130),
 ]
 
 
