@@ -12,8 +12,10 @@ from ._binding import (  # noqa: F401
     attn_bwd_gqa,
     attn_bwd_sparse,
     backward,
+    backward_host,
     check_error,
     dq_land,
+    host_scratch_size,
     library,
     preprocess,
     query_block_range,

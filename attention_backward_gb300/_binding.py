@@ -54,6 +54,9 @@ _SIGS = {
     "attn_bwd_gqa_noalloc": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides,
                                      c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32,
                                      ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp]),
+    "attn_bwd_host_scratch_size": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64, c_i64]),
+    "attn_bwd_gqa_host": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32,
+                                  ctypes.POINTER(Mask), c_vp, c_vp, c_vp, c_vp, c_sz, c_i64, c_vp, c_vp, c_vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -287,4 +290,49 @@ def backward_noalloc(q, k, v, o, do, lse, sm_scale: Optional[float] = None, caus
                                            _lse_strides(lse), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
                                            ctypes.byref(m), dq.data_ptr(), _bshd(dq), dk.data_ptr(), _bshd(dk),
                                            dv.data_ptr(), _bshd(dv), _stream(stream)), "attn_bwd_gqa_noalloc")
+    return dq, dk, dv
+
+
+def host_scratch_size(B: int, S: int, HQ: int, HKV: int, D: int, chunks: int) -> int:
+    """Device scratch bytes of attn_bwd_gqa_host."""
+    return int(library().attn_bwd_host_scratch_size(B, S, HQ, HKV, D, chunks))
+
+
+def backward_host(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1,
+                  cu_seqlens=None, chunks: int = 4, out=None, scratch=None, streams=None, device=None,
+                  sync: bool = True):
+    """dQ, dK, dV from host tensors to host tensors through attn_bwd_gqa_host,
+    the copies overlapped with the kernels chunk by chunk.
+
+    q, k, v, o, do, lse: contiguous CPU tensors (page-locked for overlap);
+    cu_seqlens: a CUDA int32 tensor or None.  ``out`` (dq, dk, dv), ``scratch``
+    (a CUDA uint8 tensor) and ``streams`` (compute, copy-in, copy-out) may be
+    passed to reuse them across calls.  Returns after the work completes, or,
+    with ``sync=False``, once it is queued (``streams[0]`` then covers it)."""
+    for t in (q, k, v, o, do, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise AttnBwdError("backward_host takes contiguous host tensors")
+    B, S, HQ, D = q.shape
+    HKV = k.shape[2]
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if out is None:
+        out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v))
+    need = host_scratch_size(B, S, HQ, HKV, D, chunks)
+    if need == 0:
+        raise AttnBwdError("attn_bwd_gqa_host: unsupported shape")
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=device)
+    if streams is None:
+        streams = (torch.cuda.current_stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device))
+    m = _mask(causal, window, cu_seqlens)
+    dq, dk, dv = out
+    _status(library().attn_bwd_gqa_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                        lse.data_ptr(), B, S, HQ, HKV, D, _dt(q), float(sm_scale), ctypes.byref(m),
+                                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), scratch.data_ptr(),
+                                        scratch.numel(), int(chunks), _stream(streams[0]), _stream(streams[1]),
+                                        _stream(streams[2])), "attn_bwd_gqa_host")
+    if sync:
+        streams[0].synchronize()
     return dq, dk, dv

@@ -316,10 +316,12 @@ def _stage_times(per):
             "ms_land": float(np.mean([e[2].elapsed_time(e[3]) for e in per]))}
 
 
-def time_e2e(w, tensors, steps, device):
+def time_e2e(w, tensors, steps, device, chunks=4):
     """The same backward through the public API with pinned host buffers:
     host->device copies of the inputs and device->host copies of the gradients
-    inside the timed region."""
+    inside the timed region.  Dense: attn_bwd_gqa_host, which pipelines the
+    copies with the kernels chunk by chunk of KV heads.  Sparse: the copies,
+    then the three launches."""
     import torch
 
     import attention_backward_gb300 as ab
@@ -329,26 +331,28 @@ def time_e2e(w, tensors, steps, device):
         host_in = [t.cpu().pin_memory() for t in tensors]           # q, kv, o, do, lse, idx
         outs = (tensors[0], tensors[1])                             # dq like q, dkv like kv
         ws = ab._binding.new_workspace(w.B, w.S, w.HQ, 0, tensors[1].numel(), device=device)
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_in]
+
+        def one():
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            grads = ab.sparse_backward(*dev_in, w.sm_scale, w.Dv, workspace=ws, stream=stream)
+            for h, d in zip(host_out, grads):
+                h.copy_(d, non_blocking=True)
     else:
-        host_in = [t.cpu().pin_memory() for t in tensors[:6]]       # q, k, v, o, do, lse
-        outs = tensors[:3]
-        ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
+        host_in = [t.cpu().contiguous().pin_memory() for t in tensors[:6]]  # q, k, v, o, do, lse
         cu = tensors[6]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in host_in[:3]]
+        scratch = torch.empty(ab.host_scratch_size(w.B, w.S, w.HQ, w.HKV, w.D, chunks), dtype=torch.uint8,
+                              device=device)
+        streams = (stream, torch.cuda.Stream(device), torch.cuda.Stream(device))
+
+        def one():
+            ab.backward_host(*host_in, w.sm_scale, w.causal, w.window, cu, chunks=chunks, out=host_out,
+                             scratch=scratch, streams=streams, device=device, sync=False)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_in]
-
-    def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        if w.kind == "sparse":
-            grads = ab.sparse_backward(*dev_in, w.sm_scale, w.Dv, workspace=ws, stream=stream)
-        else:
-            grads = ab.backward(*dev_in, w.sm_scale, causal=w.causal, window=w.window, cu_seqlens=cu,
-                                workspace=ws, stream=stream)
-        for h, d in zip(host_out, grads):
-            h.copy_(d, non_blocking=True)
 
     one()
     torch.cuda.synchronize(device)

@@ -226,6 +226,44 @@ ATTN_BWD_API attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq
                                                 const attn_mask_t* mask, void* dq, attn_strides_t sdq, void* dk,
                                                 attn_strides_t sdk, void* dv, attn_strides_t sdv, void* stream);
 
+/* Device scratch bytes that attn_bwd_gqa_host needs to process the problem
+ * in ``chunks`` chunks of KV heads (0 for an invalid shape). */
+ATTN_BWD_API size_t attn_bwd_host_scratch_size(int64_t B, int64_t S, int64_t HQ, int64_t HKV, int64_t D,
+                                               int64_t chunks);
+
+/* The dense backward from host buffers to host buffers, with the
+ * host<->device copies overlapped with the kernels.  This entry point is a
+ * convenience of this library; the pages it follows have no counterpart.
+ *
+ * The problem is split into ceil(HKV / ceil(HKV / chunks)) chunks of KV heads;
+ * a chunk and its query heads are independent of the others.  Each chunk is
+ * copied in (strided head slices of the host tensors into contiguous device
+ * buffers, on ``copy_in_stream``), run through attn_bwd_preprocess,
+ * attn_bwd_gqa and attn_bwd_dq_land (on ``stream``) and copied out (on
+ * ``copy_out_stream``), with two buffer slots so that copies of neighbouring
+ * chunks overlap the kernels.  The copies start after the work queued on
+ * ``stream`` before the call, and ``stream`` waits for the last copy-out, so
+ * synchronising ``stream`` covers the whole call.  The three streams must be
+ * distinct for the work to overlap.
+ *   q, o, dO, dq : host [B,S,HQ,D] 16-bit, contiguous;  k, v, dk, dv : host
+ *   [B,S,HKV,D] 16-bit, contiguous;  lse : host f32 [B,HQ,S] (natural log),
+ *   contiguous.  Host buffers should be page-locked (with pageable memory the
+ *   copies are correct but do not overlap); dq, dk, dv are written.
+ *   mask : as for attn_bwd_gqa (cu_seqlens in device memory).
+ *   scratch : device memory of attn_bwd_host_scratch_size(...) bytes, 256-byte
+ *   aligned, owned by the caller; it starts with the workspace of one chunk,
+ *   so attn_bwd_check_error(scratch, stream, ...) reports device errors.
+ * The call creates CUDA events and releases them before it returns (each is
+ * freed once the work that uses it completes); it allocates no memory.
+ * Returns an error before queueing anything for invalid arguments; an error
+ * from a later step leaves the chunks queued so far in flight. */
+ATTN_BWD_API attn_status_t attn_bwd_gqa_host(const void* q, const void* k, const void* v, const void* o,
+                                             const void* dO, const float* lse, int64_t B, int64_t S, int64_t HQ,
+                                             int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
+                                             const attn_mask_t* mask, void* dq, void* dk, void* dv, void* scratch,
+                                             size_t scratch_bytes, int64_t chunks, void* stream,
+                                             void* copy_in_stream, void* copy_out_stream);
+
 #ifdef __cplusplus
 }
 #endif
