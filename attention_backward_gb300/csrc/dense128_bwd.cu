@@ -22,7 +22,8 @@
 // drop by a quarter and the tensor pipe can run at full rate.
 //
 // Tensor memory (512 columns): S^T [128 x 128] f32 at 0, overwritten by P^T
-// (16-bit pairs, columns 0-63) and dS^T (columns 64-127); dP^T at 128, which
+// and dS^T as 16-bit pairs, each softmax warpgroup in its own 64 columns (P^T
+// in the first 32, dS^T in the last 32); dP^T at 128, which
 // the f32 dQ of the step overwrites once the softmax warps have read dP; dV at
 // 256, dK at 384.
 //
@@ -92,7 +93,6 @@ enum Bar : int {
   TILE_EMPTY0 = 8,  // 2 slots
   S_FULL = 10,
   S_FREE,           // dV and dK of the step completed: S^T columns reusable
-  SREAD,            // 8 softmax warps finished reading S^T
   P_READY,          // 8 softmax warps stored P^T
   DP_FULL,
   DS_READY,         // 8 softmax warps stored dS^T (TMEM) and dS (shared)
@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     }
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[S_FREE], 1);
-    mbar_init(&bars[SREAD], 8);
     mbar_init(&bars[P_READY], 8);
     mbar_init(&bars[DP_FULL], 1);
     mbar_init(&bars[DS_READY], 8);
@@ -312,13 +311,13 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_w(tmem + T_DV, tmem + T_S + kk * 8, dO_mn + so + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
+          mma_ts_w(tmem + T_DV, tmem + T_S + pair_col(kk * 16, BN / 2), dO_mn + so + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
         // ---- dK += dS^T Q
         if (!(ok = mbar_wait_warp(&bars[DS_READY], gs & 1, wc, kErrWaitDS))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_w(tmem + T_DK, tmem + T_S + BN / 2 + kk * 8, dQ_mn + so + sdesc_step(kk * 2048), IDESC_KV,
+          mma_ts_w(tmem + T_DK, tmem + T_S + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + so + sdesc_step(kk * 2048), IDESC_KV,
                    j > 0 || kk > 0);
         mma_commit_w(&bars[S_FREE]);
         // ---- dQ = dS K over the 128 key rows (A = dS MN-major in two 64-query blocks, B = K MN-major),
@@ -404,19 +403,14 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
             }
           }
         }
-        // P^T overwrites S^T columns the other warpgroup reads: all eight
-        // warps finish reading S^T first.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[SREAD]);
-        if (!(ok = mbar_wait_warp(&bars[SREAD], gs & 1, wc, kErrWaitSRead))) break;
-        tc_fence_after();
+        // P^T pairs go into the first half of this warpgroup's own S^T columns,
+        // which only this warp's lanes read (and its loads have completed)
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t w[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
-          tmem_st16(sb + (wg * HALF + ch * 32) / 2, w);
+          tmem_st16(sb + wg * HALF + ch * 16, w);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -442,9 +436,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
             const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dl.y);
             dsw[c / 2] = pack2<BF16>(d0, d1);
           }
-          // dS^T pairs into columns 64-127 (the S^T there is read), and dS as the
-          // MN-major A operand of dQ: 64-query block wg, row = key, 16-byte chunks 4ch..4ch+3
-          tmem_st16(sb + BN / 2 + (wg * HALF + ch * 32) / 2, dsw);
+          // dS^T pairs into the second half of this warpgroup's S^T columns, and dS
+          // as the MN-major A operand of dQ: 64-query block wg, row = key, 16-byte chunks 4ch..4ch+3
+          tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
             *reinterpret_cast<uint4*>(dsb + sw128_offset(row, ch * 4 + c4)) =

@@ -101,9 +101,8 @@ enum Bar : int {
   TILE_EMPTY0 = 10, // 2 slots
   S_FULL0 = 12,     // 2 buffers
   S_FREE0 = 14,     // 2 buffers
-  SREAD = 16,
-  P_READY0,  // 2 buffers
-  DP_FULL = 19,
+  P_READY0 = 16,  // 2 buffers
+  DP_FULL = 18,
   DS_READY,
   DS_SFREE0,  // NDS buffers (up to 2)
   DQ_FULL = DS_SFREE0 + 2,
@@ -148,7 +147,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       mbar_init(&bars[S_FULL0 + i], 1);
       mbar_init(&bars[S_FREE0 + i], 1);
     }
-    mbar_init(&bars[SREAD], 8);
     mbar_init(&bars[P_READY0], 8);
     mbar_init(&bars[P_READY0 + 1], 8);
     mbar_init(&bars[DP_FULL], 1);
@@ -358,7 +356,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_w(tmem + C::T_DV, sb + kk * 8, dO_mn + qo + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
+          mma_ts_w(tmem + C::T_DV, sb + pair_col(kk * 16, BN / 2), dO_mn + qo + sdesc_step(kk * 2048), IDESC_KV,
+                   j > 0 || kk > 0);
         // ---- dP^T of the next step, as soon as this step's dP^T has been loaded
         if (j + 1 < n) {
           if (!(ok = mbar_wait_warp(&bars[DP_FREE], cur & 1, wc, kErrWaitDP))) break;
@@ -377,7 +376,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_w(tmem + C::T_DK, sb + BN / 2 + kk * 8, dQ_mn + qo + sdesc_step(kk * 2048), IDESC_KV, j > 0 || kk > 0);
+          mma_ts_w(tmem + C::T_DK, sb + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + qo + sdesc_step(kk * 2048),
+                   IDESC_KV, j > 0 || kk > 0);
         mma_commit_w(&bars[EMPTY0 + st]);  // every reader of this Q/dO stage issued
         uint32_t dq_cols;
         if constexpr (D == 128) {
@@ -506,19 +506,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             }
           }
         }
-        // P^T overwrites S^T columns the other warpgroup reads: all eight
-        // warps finish reading S^T first.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[SREAD]);
-        if (!(ok = mbar_wait_warp(&bars[SREAD], gs & 1, wc, kErrWaitSRead))) break;
-        tc_fence_after();
+        // P^T pairs go into the first half of this warpgroup's own S^T columns,
+        // which only this warp's lanes read (and its loads have completed)
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t w[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
-          tmem_st16(sb + (wg * HALF + ch * 32) / 2, w);
+          tmem_st16(sb + wg * HALF + ch * 16, w);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -563,8 +558,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             if (!(ok = ds_tile_free())) break;
             tc_fence_after();
           }
-          // dS^T into the second half of this step's S^T buffer (its S^T is read)
-          tmem_st16(sb + BN / 2 + (wg * HALF + ch * 32) / 2, dsw);
+          // dS^T pairs into the second half of this warpgroup's S^T columns
+          tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
           if constexpr (D == 128) {
             // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
             // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``

@@ -10,6 +10,16 @@ struct TileInfo {
   int b, g, seq_start, len, k0, qlo, nq, valid;
 };
 
+// TMEM column, relative to a step's S^T buffer, of the 16-bit pair of P^T
+// that holds query q (q even; the pair is queries q, q + 1).  Each softmax
+// warpgroup owns ``half`` consecutive query columns of S^T and writes its P^T
+// pairs into the first half of them and its dS^T pairs (same offset plus
+// half / 2) into the second half, so no warp overwrites columns that another
+// warp still has to read.  A K-step of 16 queries is 8 consecutive columns.
+__host__ __device__ constexpr uint32_t pair_col(int q, int half) {
+  return static_cast<uint32_t>((q / half) * half + (q % half) / 2);
+}
+
 // Tile t -> (batch, KV head, key block); longest tiles first (smallest key
 // block index first, which is the longest under a causal mask).
 static __device__ __forceinline__ TileInfo decode_tile(int t, const DenseParams& p) {
