@@ -255,6 +255,7 @@ attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t 
                                void* stream) {
   if (!dq || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1 || D < 8 || D % 8) return ATTN_ERR_INVALID_ARG;
+  if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(dq) || !aligned16(workspace) || !strides_ok(sdq)) return ATTN_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(B, S, H, D, 0);
@@ -323,6 +324,7 @@ attn_status_t attn_bwd_sparse_land(void* dkv, attn_strides_t sdkv, int64_t B, in
                                    size_t workspace_bytes, void* stream) {
   if (!dkv || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || DQK < 8 || DQK % 8) return ATTN_ERR_INVALID_ARG;
+  if (B * SKV * HKV >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(dkv) || !aligned16(workspace) || !strides_ok(sdkv)) return ATTN_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(B, S, H, 0, B * SKV * HKV * DQK);

@@ -55,7 +55,13 @@ template <int D>
 struct Cfg {
   static constexpr int BM = kDenseBM;
   static constexpr int BN = dense_bn(D);
-  static constexpr int STAGES = 3;
+  // Head dim 64 stages the f32 dQ partial of a step in the step's own Q/dO
+  // stage once its MMAs are done, which leaves room for a second dS tile.
+  // Head dim 128 keeps a separate staging buffer: there the stage would be
+  // released later than the dK MMA releases it, which was measured slower
+  // even with a fourth stage in the freed space.
+  static constexpr bool STG_IN_STAGE = D == 64;
+  static constexpr int STAGES = 3;  // the barrier layout below holds up to 3
   static constexpr int PREFETCH = 8;  // L2 prefetch distance of Q/dO/LSE/delta, in steps
   static constexpr int NSLAB = D / 64;  // 64-column (128-byte) slabs per row
   static constexpr int KV_SLAB = BM * 128;
@@ -63,8 +69,9 @@ struct Cfg {
   static constexpr int Q_SLAB = BN * 128;
   static constexpr int Q_TILE = Q_SLAB * NSLAB;
   static constexpr int DS_BYTES = BM * BN * 2;
-  static constexpr int NDS = D == 128 ? 2 : 1;  // dS tiles in shared memory (double-buffered when they fit)
-  static constexpr int STG_BYTES = BN * D * 4;  // f32 dQ staging of one step
+  static constexpr int NDS = 2;  // dS tiles in shared memory (double-buffered)
+  static constexpr int STG_BYTES = STG_IN_STAGE ? 0 : BN * D * 4;  // separate f32 dQ staging
+  static_assert(BN * D * 4 == 2 * Q_TILE, "the f32 dQ staging of a step fills a Q/dO stage");
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
@@ -78,8 +85,9 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_RING + 64;
   static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static constexpr int SMEM = OFF_MISC + 64;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   // tensor memory columns (512 allocated)
   static constexpr int T_SB = 0;           // two S^T buffers [128 x BN] f32; P^T / dS^T (16-bit pairs) overwrite them
   static constexpr int T_DP = 2 * BN;      // dP^T f32 [128 x BN]
@@ -93,22 +101,22 @@ struct Cfg {
 };
 
 enum Bar : int {
-  FULL0 = 0,   // 3 stages
-  EMPTY0 = 3,  // 3 stages
+  FULL0 = 0,        // 3 stages
+  EMPTY0 = 3,       // 3 stages: every reader of the stage is done
   KV_FULL = 6,
   KV_FREE,
-  TILE_FULL0,       // 2 slots
+  TILE_FULL0 = 8,   // 2 slots
   TILE_EMPTY0 = 10, // 2 slots
   S_FULL0 = 12,     // 2 buffers
   S_FREE0 = 14,     // 2 buffers
-  P_READY0 = 16,  // 2 buffers
+  P_READY0 = 16,    // 2 buffers
   DP_FULL = 18,
   DS_READY,
-  DS_SFREE0,  // NDS buffers (up to 2)
+  DS_SFREE0,        // 2 dS tiles
   DQ_FULL = DS_SFREE0 + 2,
   DQ_EMPTY,
-  STG_FREE,
-  STG_FULL,
+  STG_FULL,         // 4 epilogue warps wrote their staging rows
+  STG_FREE,         // the separate staging buffer has been read by the previous reduce
   DKV_FULL,
   DKV_FREE,
   DRAIN,
@@ -122,8 +130,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
   using C = Cfg<D>;
   constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES, kPrefetch = C::PREFETCH;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   TileInfo* ring = reinterpret_cast<TileInfo*>(sm + C::OFF_RING);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
@@ -132,6 +139,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   float* s_delta = reinterpret_cast<float*>(sm + C::OFF_DELTA);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  if ((smem_u32(sm) & 1023u) != 0) {  // the swizzled tiles need an aligned base
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrAlign);
+    return;
+  }
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -155,8 +166,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[DS_SFREE0 + 1], 1);
     mbar_init(&bars[DQ_FULL], 1);
     mbar_init(&bars[DQ_EMPTY], 4);
-    mbar_init(&bars[STG_FREE], 1);
     mbar_init(&bars[STG_FULL], 4);
+    mbar_init(&bars[STG_FREE], 1);
     mbar_init(&bars[DKV_FULL], 1);
     mbar_init(&bars[DKV_FREE], 8);
     mbar_init(&bars[DRAIN], 1);
@@ -378,7 +389,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_w(tmem + C::T_DK, sb + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + qo + sdesc_step(kk * 2048),
                    IDESC_KV, j > 0 || kk > 0);
-        mma_commit_w(&bars[EMPTY0 + st]);  // every reader of this Q/dO stage issued
+        // with a separate staging buffer, the dK MMA is the last reader of the stage
+        if constexpr (!C::STG_IN_STAGE) mma_commit_w(&bars[EMPTY0 + st]);
         uint32_t dq_cols;
         if constexpr (D == 128) {
           mma_commit_w(&bars[S_FREE0 + (cur & 1)]);  // P^T / dS^T of this buffer consumed
@@ -399,7 +411,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             mma_ss_w(dq_cols, dK_mn + sdesc_step(kk * 2048),
                      dDS_mn + sdesc_step((cur % C::NDS) * C::DS_BYTES + kk * 2048), IDESC_DQ, kk > 0);
           else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
-            mma_ss_w(dq_cols, dDS_mn + sdesc_step(kk * 2048), dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
+            mma_ss_w(dq_cols, dDS_mn + sdesc_step((cur % C::NDS) * C::DS_BYTES + kk * 2048),
+                     dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
         }
         mma_commit_w(&bars[DQ_FULL]);
         mma_commit_w(&bars[DS_SFREE0 + cur % C::NDS]);
@@ -570,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
                   make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
           } else {
             // dS as the MN-major A operand: 64-query block wg, row = key, chunks 4ch .. 4ch+3
-            uint8_t* base = sm + C::OFF_DS + wg * (BM * 128);
+            uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES + wg * (BM * 128);
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4)
               *reinterpret_cast<uint4*>(base + sw128_offset(row, ch * 4 + c4)) =
@@ -624,9 +637,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     }
   } else {
     // ============================================================ dQ epilogue
+    // Head dim 64: the f32 dQ partial of a step is staged in the step's own
+    // Q/dO stage (every MMA reading the stage was issued before dQ, so it has
+    // completed once DQ_FULL has), one 128-byte-swizzled [128 q x 32 d] slab in
+    // the Q part and one in the dO part, and the stage is handed back to the
+    // producer once the two bulk tensor reduce-adds have read it.  Head dim 128:
+    // staged as [64 q x 128 d] in the separate buffer, which is reused once the
+    // previous reduce has read it.
     const int quad = warp;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    float* stg = reinterpret_cast<float*>(sm + C::OFF_STG);
     const bool leader = warp == 0 && lane == 0;
     bool issued = false;
     uint32_t gs = 0;
@@ -640,6 +659,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       if (!ti.valid) break;
       const int n = p.G * ti.nq;
       for (int j = 0; j < n; ++j, ++gs) {
+        const int st = gs % ST;
         const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
         if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
@@ -651,27 +671,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[DQ_EMPTY]);
-        // the staging buffer is free once the previous bulk reduce has read it
-        if (leader) {
-          if (issued) bulk_wait_read_all();
-          mbar_arrive(&bars[STG_FREE]);
-        }
-        if (!(ok = mbar_wait_warp(&bars[STG_FREE], gs & 1, wc, kErrWaitStage))) break;
-        if constexpr (D == 128) {
+        uint8_t* const half0 = sm + C::OFF_Q + st * C::Q_TILE;
+        uint8_t* const half1 = sm + C::OFF_DO + st * C::Q_TILE;
+        float* const stg = reinterpret_cast<float*>(sm + C::OFF_STG);
+        if constexpr (C::STG_IN_STAGE) {
+          // lane = query; half c / 8 is a 128-byte-swizzled slab [128 q][32 d]
+          const int q = quad * 32 + lane;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            uint8_t* slab = c < 8 ? half0 : half1;
+            *reinterpret_cast<float4*>(slab + sw128_offset(q, c & 7)) =
+                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
+                            __uint_as_float(r[4 * c + 3]));
+          }
+        } else {
+          // the separate staging buffer is free once the previous reduce has read it
+          if (leader) {
+            if (issued) bulk_wait_read_all();
+            mbar_arrive(&bars[STG_FREE]);
+          }
+          if (!(ok = mbar_wait_warp(&bars[STG_FREE], gs & 1, wc, kErrWaitStage))) break;
           // lane = head dim d; staging [64 queries][128 d] f32, rows of 512 bytes
           const int d = quad * 32 + lane;
 #pragma unroll
           for (int c = 0; c < 64; ++c) stg[c * 128 + d] = __uint_as_float(r[c]);
-        } else {
-          // lane = query; staging = two 128-byte-swizzled slabs [128 q][32 d]
-          const int q = quad * 32 + lane;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int slab = c >> 3, chunk = c & 7;
-            *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(stg) + slab * (128 * 128) + sw128_offset(q, chunk)) =
-                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
-                            __uint_as_float(r[4 * c + 3]));
-          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -681,13 +704,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           lok = mbar_wait(&bars[STG_FULL], gs & 1, wc, kErrWaitStage);
           if (lok) {
             const int c2 = ti.seq_start + q0;
-            if constexpr (D == 128) {
-              tma_reduce_add_4d(&maps.dq, stg, 0, h, c2, ti.b);
+            if constexpr (C::STG_IN_STAGE) {
+              tma_reduce_add_4d(&maps.dq, half0, 0, h, c2, ti.b);
+              tma_reduce_add_4d(&maps.dq, half1, D / 2, h, c2, ti.b);
+              bulk_commit_group();
+              bulk_wait_read_all();  // the stage may be reloaded once the reduces have read it
+              mbar_arrive(&bars[EMPTY0 + st]);
             } else {
               tma_reduce_add_4d(&maps.dq, stg, 0, h, c2, ti.b);
-              tma_reduce_add_4d(&maps.dq, reinterpret_cast<uint8_t*>(stg) + 128 * 128, 32, h, c2, ti.b);
+              bulk_commit_group();
             }
-            bulk_commit_group();
             issued = true;
           }
         }

@@ -33,76 +33,141 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   }
 }
 
+// Lanes per row (a power of two, at most 32) for rows of ``chunks`` 16-byte
+// chunks; a warp covers 32 / lanes rows at a time.
+__device__ __forceinline__ int lanes_per_row(int chunks) {
+  int g = 1;
+  while (g * 2 <= chunks && g * 2 <= 32) g *= 2;
+  return g;
+}
+
+// Rows of each lane group handled per loop iteration: their loads are all
+// issued before any of them is used, so that enough bytes are in flight to
+// cover the memory latency.
+constexpr int kRowsInFlight = 4;
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) preprocess_kernel(PreprocessParams p) {
-  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // grid x block < 2^31 and B*H*S < 2^31 (checked on the host): 32-bit indices
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthr = gridDim.x * blockDim.x;
   if (gtid == 0) {
     p.hdr->err = 0;
     p.hdr->tile_counter = 0;
   }
   for (int64_t i = gtid; i < p.zero_n4; i += nthr) p.zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.S;
-  for (int64_t r = gtid; r < rows; r += nthr) {
-    const int64_t s = r % p.S, h = (r / p.S) % p.H, b = r / (static_cast<int64_t>(p.S) * p.H);
+  const int rows = p.B * p.H * p.S;
+  for (int r = gtid; r < rows; r += nthr) {
+    const int s = r % p.S, t = r / p.S, h = t % p.H, b = t / p.H;
     p.lse2[r] = p.lse[b * p.sl_b + h * p.sl_h + s * p.sl_s] * kLog2e;
   }
 
   // delta: a group of ``gs`` lanes per (b, s, h) row, rows ordered (b, s, h)
   // so that consecutive groups read consecutive memory.
+  constexpr int U = kRowsInFlight;
   const int chunks = p.Dv / 8;
-  int gs = 1;
-  while (gs * 2 <= chunks && gs * 2 <= 32) gs *= 2;
+  const int gs = lanes_per_row(chunks);
   const int lane = threadIdx.x & 31;
-  const int64_t warp = gtid >> 5, nwarps = nthr >> 5;
+  const int warp = gtid >> 5, nwarps = nthr >> 5;
   const int rows_per_warp = 32 / gs;
   const int sub = lane / gs, lig = lane % gs;
-  for (int64_t base = warp * rows_per_warp; base < rows; base += nwarps * rows_per_warp) {
-    const int64_t r = base + sub;
-    float acc = 0.f;
-    int64_t b = 0, s = 0, h = 0;
-    if (r < rows) {
-      h = r % p.H;
-      s = (r / p.H) % p.S;
-      b = r / (static_cast<int64_t>(p.H) * p.S);
-      // the row's dQ accumulator (same (b, s, h) order), so that its writes
-      // overlap the O/dO reads
-      float4* z = p.dq_zero + r * p.dq_row_n4;
-      for (int k = lig; k < p.dq_row_n4; k += gs) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      const uint4* o = reinterpret_cast<const uint4*>(p.o + 2 * (b * p.so_b + s * p.so_s + h * p.so_h));
-      const uint4* d = reinterpret_cast<const uint4*>(p.dO + 2 * (b * p.sdo_b + s * p.sdo_s + h * p.sdo_h));
-      for (int c = lig; c < chunks; c += gs) {
-        float fo[8], fd[8];
-        unpack8<BF16>(__ldg(o + c), fo);
-        unpack8<BF16>(__ldg(d + c), fd);
+  const int span = rows_per_warp * U;
+  for (int base = warp * span; base < rows; base += nwarps * span) {
+    const uint4* op[U];
+    const uint4* dp[U];
+    int64_t di[U];
+    float acc[U];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(fo[e], fd[e], acc);
+    for (int k = 0; k < U; ++k) {
+      const int r = base + k * rows_per_warp + sub;
+      acc[k] = 0.f;
+      op[k] = dp[k] = nullptr;
+      di[k] = -1;
+      if (r < rows) {
+        const int h = r % p.H, t = r / p.H, s = t % p.S, b = t / p.S;
+        op[k] = reinterpret_cast<const uint4*>(p.o + 2 * (b * p.so_b + s * p.so_s + h * p.so_h));
+        dp[k] = reinterpret_cast<const uint4*>(p.dO + 2 * (b * p.sdo_b + s * p.sdo_s + h * p.sdo_h));
+        di[k] = (static_cast<int64_t>(b) * p.H + h) * p.S + s;
       }
     }
-    for (int off = gs / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (r < rows && lig == 0) p.delta[(b * p.H + h) * p.S + s] = acc;
+    for (int c = lig; c < chunks; c += gs) {
+      uint4 ou[U], du[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        ou[k] = du[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (op[k] != nullptr) {
+          ou[k] = __ldg(op[k] + c);
+          du[k] = __ldg(dp[k] + c);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        float fo[8], fd[8];
+        unpack8<BF16>(ou[k], fo);
+        unpack8<BF16>(du[k], fd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[k] = fmaf(fo[e], fd[e], acc[k]);
+      }
+    }
+    // the rows' dQ accumulators (same (b, s, h) order); their writes overlap
+    // the O/dO reads of the next iteration
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int r = base + k * rows_per_warp + sub;
+      if (r < rows) {
+        float4* z = p.dq_zero + static_cast<int64_t>(r) * p.dq_row_n4;
+        for (int q = lig; q < p.dq_row_n4; q += gs) z[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      for (int off = gs / 2; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+      if (di[k] >= 0 && lig == 0) p.delta[di[k]] = acc[k];
+    }
   }
 }
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) land_kernel(LandParams p) {
-  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // rows = B*S*H < 2^31 (checked on the host); a group of ``gs`` lanes per row
+  constexpr int U = kRowsInFlight;
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthr = gridDim.x * blockDim.x;
   const int cpr = p.D / 8;  // 8-element chunks per row
-  const int64_t n = p.rows * cpr;
-  for (int64_t i = gtid; i < n; i += nthr) {
-    const int64_t row = i / cpr;
-    const int c = static_cast<int>(i % cpr);
-    const int64_t h = row % p.H, s = (row / p.H) % p.S, b = row / (static_cast<int64_t>(p.H) * p.S);
-    const float4* a = reinterpret_cast<const float4*>(p.acc + row * p.D + c * 8);
-    const float4 x = a[0], y = a[1];
-    uint4 o;
-    o.x = pack2<BF16>(x.x * p.scale, x.y * p.scale);
-    o.y = pack2<BF16>(x.z * p.scale, x.w * p.scale);
-    o.z = pack2<BF16>(y.x * p.scale, y.y * p.scale);
-    o.w = pack2<BF16>(y.z * p.scale, y.w * p.scale);
-    *reinterpret_cast<uint4*>(p.out + 2 * (b * p.s_b + s * p.s_s + h * p.s_h + c * 8)) = o;
+  const int gs = lanes_per_row(cpr);
+  const int lane = threadIdx.x & 31;
+  const int warp = gtid >> 5, nwarps = nthr >> 5;
+  const int rows_per_warp = 32 / gs;
+  const int sub = lane / gs, lig = lane % gs;
+  const int span = rows_per_warp * U;
+  const int rows = static_cast<int>(p.rows);
+  for (int base = warp * span; base < rows; base += nwarps * span) {
+    for (int c = lig; c < cpr; c += gs) {
+      float4 x[U], y[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int r = base + k * rows_per_warp + sub;
+        if (r < rows) {
+          const float4* a = reinterpret_cast<const float4*>(p.acc + static_cast<int64_t>(r) * p.D + c * 8);
+          x[k] = a[0];
+          y[k] = a[1];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int r = base + k * rows_per_warp + sub;
+        if (r < rows) {
+          const int h = r % p.H, t = r / p.H, s = t % p.S, b = t / p.S;
+          uint4 o;
+          o.x = pack2<BF16>(x[k].x * p.scale, x[k].y * p.scale);
+          o.y = pack2<BF16>(x[k].z * p.scale, x[k].w * p.scale);
+          o.z = pack2<BF16>(y[k].x * p.scale, y[k].y * p.scale);
+          o.w = pack2<BF16>(y[k].z * p.scale, y[k].w * p.scale);
+          *reinterpret_cast<uint4*>(p.out + 2 * (b * p.s_b + s * p.s_s + h * p.s_h + c * 8)) = o;
+        }
+      }
+    }
   }
 }
 

@@ -133,7 +133,8 @@ ATTN_BWD_API attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void
                        void* stream);
 
 /* Launch 3: dQ = cast(sm_scale * dQacc), the TileOPs page's "dq_land".
- *   dq : [B,S,H,D] 16-bit (written). */
+ *   dq : [B,S,H,D] 16-bit (written).  B*S*H below 2^31, else
+ *   ATTN_ERR_UNSUPPORTED. */
 ATTN_BWD_API attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
                                attn_dtype_t dtype, float sm_scale, const void* workspace, size_t workspace_bytes,
                                void* stream);
@@ -166,7 +167,8 @@ ATTN_BWD_API attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, con
  * sm_scale to dS itself: dKV mixes the scaled dK term with the unscaled dV
  * term, so the scale cannot be folded into a landing pass as on the dense
  * path).  B, S, H locate the workspace regions as at preprocess time.
- *   dkv : [B,SKV,HKV,DQK] 16-bit (written). */
+ *   dkv : [B,SKV,HKV,DQK] 16-bit (written).  B*SKV*HKV below 2^31, else
+ *   ATTN_ERR_UNSUPPORTED. */
 ATTN_BWD_API attn_status_t attn_bwd_sparse_land(void* dkv, attn_strides_t sdkv, int64_t B, int64_t S, int64_t SKV,
                                                 int64_t H, int64_t HKV, int64_t DQK, attn_dtype_t dtype,
                                                 const void* workspace, size_t workspace_bytes, void* stream);
