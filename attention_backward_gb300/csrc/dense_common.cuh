@@ -20,15 +20,38 @@ __host__ __device__ constexpr uint32_t pair_col(int q, int half) {
   return static_cast<uint32_t>((q / half) * half + (q % half) / 2);
 }
 
+// (batch, KV head) pairs whose tiles are drawn together (dense batches).
+constexpr int kTileGroup = 16;
+
 // Tile t -> (batch, KV head, key block); longest tiles first (smallest key
-// block index first, which is the longest under a causal mask).
+// block index first, which is the longest under a causal mask).  Dense
+// batches go through the (batch, KV head) pairs in groups of kTileGroup,
+// key block major inside a group: the CTAs in flight then share the Q/dO rows
+// and dQ accumulator rows of a few heads, which stay in L2, at no cost in
+// load balance (each group still ends with its shortest tiles).  Packed
+// sequences keep key block major order over all pairs (their tile count per
+// pair is known only on the device, and the draws past it end a CTA's work).
 static __device__ __forceinline__ TileInfo decode_tile(int t, const DenseParams& p) {
   TileInfo ti{};
   ti.valid = 0;
   const int BH = p.B * p.HKV;
   if (t < 0) return ti;
-  const int bh = t % BH;
-  int r = t / BH;
+  int bh, r;
+  if (p.cu_seqlens == nullptr) {
+    const int nt = (p.S + kDenseBM - 1) / kDenseBM;  // key tiles per pair
+    const int grp = imin(BH, kTileGroup);
+    const int gi = t / (grp * nt);
+    const int g0 = gi * grp;
+    if (g0 >= BH) return ti;
+    const int gn = imin(grp, BH - g0);  // the last group may hold fewer pairs
+    const int u = t - gi * grp * nt;
+    if (u >= gn * nt) return ti;
+    bh = g0 + u % gn;
+    r = u / gn;
+  } else {
+    bh = t % BH;
+    r = t / BH;
+  }
   ti.b = bh / p.HKV;
   ti.g = bh % p.HKV;
   if (p.cu_seqlens != nullptr) {
@@ -46,7 +69,6 @@ static __device__ __forceinline__ TileInfo decode_tile(int t, const DenseParams&
     }
     if (!found) return ti;
   } else {
-    if (static_cast<int64_t>(r) * kDenseBM >= p.S) return ti;
     ti.seq_start = 0;
     ti.len = p.S;
   }
