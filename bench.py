@@ -489,7 +489,7 @@ def describe(w, r, pk, pk_kind, world=1):
         achieved = flops / (ms_main * 1e-3) / 1e12
         peak = float(pk["bf16_tflops"])  # fp16 and bf16 share the nominal dense rate
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
-        if w.D == 128 and not (w.causal or w.window > 0):  # unmasked head dim 128: 128-query steps
+        if w.D == 128:  # head dim 128: 128-query steps
             kname, src = f"dense128_bwd_kernel<{w.dtype}>", _os.path.join(csrc, "dense128_bwd.cu")
         else:
             kname, src = f"dense_bwd_kernel<{w.D},{w.dtype}>", _os.path.join(csrc, "dense_bwd.cu")
