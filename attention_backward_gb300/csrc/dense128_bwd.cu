@@ -30,8 +30,9 @@
 // Shared memory: K, V (32 KB each), two Q/dO stages (64 KB each), the dS tile
 // (32 KB).  The f32 dQ of a step (64 KB) is staged in that step's own Q/dO
 // stage once dV and dK have read it, added into the workspace accumulator with
-// four TMA bulk tensor reduce-adds, and the stage is handed back to the
-// producer after the reduce has read it.
+// four TMA bulk tensor reduce-adds.  The Q half and the dO half of the stage
+// go back to the producer separately, each as soon as the reduces of its own
+// two staging slabs have read it.
 //
 // Warp roles (14 warps): 0-3 dQ epilogue (lane = query), 4-11 two warpgroups
 // of softmax/dS work (each owns 64 of the 128 query columns of all 128 key
@@ -84,14 +85,21 @@ constexpr int T_DV = 256;
 constexpr int T_DK = 384;
 constexpr int THREADS = 14 * 32;
 
+// Each stage has two halves with their own barriers: Q (with the step's LSE2
+// and delta) and dO.  The f32 dQ staging of a step covers both halves, and
+// each half goes back to the producer as soon as the reduces of its own
+// staging slabs have read it, so the next Q (needed first, by S^T and the
+// softmax) does not wait for the reduces of the dO half.
 enum Bar : int {
-  FULL0 = 0,        // ST stages: producer's expect_tx arrival + its LSE/delta arrival
-  EMPTY0 = 2,       // ST stages: the dQ reduce has read the staging in the stage
-  KV_FULL = 4,
+  FULL0 = 0,         // ST stages: Q half loaded (expect_tx arrival) + the producer's LSE/delta arrival
+  FULLD0 = 2,        // ST stages: dO half loaded
+  EMPTY0 = 4,        // ST stages: the dQ reduces have read the staging slabs in the Q half
+  EMPTYD0 = 6,       // ST stages: ... in the dO half
+  KV_FULL = 8,
   KV_FREE,
-  TILE_FULL0,       // 2 slots
-  TILE_EMPTY0 = 8,  // 2 slots
-  S_FULL = 10,
+  TILE_FULL0 = 10,   // 2 slots
+  TILE_EMPTY0 = 12,  // 2 slots
+  S_FULL = 14,
   S_FREE,           // dV and dK of the step completed: S^T columns reusable
   P_READY,          // 8 softmax warps stored P^T
   DP_FULL,
@@ -128,7 +136,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     *abort_flag = 0;
     for (int i = 0; i < ST; ++i) {
       mbar_init(&bars[FULL0 + i], 2);
+      mbar_init(&bars[FULLD0 + i], 1);
       mbar_init(&bars[EMPTY0 + i], 1);
+      mbar_init(&bars[EMPTYD0 + i], 1);
       mbar_init(&bars[STG_FULL0 + i], 4);
     }
     mbar_init(&bars[KV_FULL], 1);
@@ -162,9 +172,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
 
   if (warp == 12) {
     // ============================================================ producer
-    int pend_full[ST];
+    int pend_full[ST], pend_d[ST];
 #pragma unroll
-    for (int i = 0; i < ST; ++i) pend_full[i] = -1;
+    for (int i = 0; i < ST; ++i) pend_full[i] = pend_d[i] = -1;
     int kv_pend = -1;
     uint32_t gs = 0;
     bool ok = true;
@@ -214,13 +224,12 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
         uint8_t* sq = sm + OFF_STAGE + st * STAGE;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[FULL0 + st], STAGE);
+          mbar_arrive_expect_tx(&bars[FULL0 + st], Q_TILE);
 #pragma unroll
-          for (int s = 0; s < 2; ++s) {
+          for (int s = 0; s < 2; ++s)
             tma_load_4d(sq + s * SLAB, &maps.q, &bars[FULL0 + st], s * 64, h, ti.seq_start + q0, ti.b);
-            tma_load_4d(sq + Q_TILE + s * SLAB, &maps.dO, &bars[FULL0 + st], s * 64, h, ti.seq_start + q0, ti.b);
-          }
         }
+        pend_full[st] = r & 1;
         // warm L2 with the operands of a step PREFETCH steps ahead
         if (j + PREFETCH < n) {
           const int hf = ti.g * p.G + (j + PREFETCH) / ti.nq, qf = (ti.qlo + (j + PREFETCH) % ti.nq) * BN;
@@ -237,6 +246,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
             prefetch_l2(p.delta + rf + lane * 32);
           }
         }
+        // LSE2/delta of the stage were last read by the softmax of step gs - ST,
+        // which finished before that step's dQ (and so before EMPTY0)
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
           s_lse[st * BN + lane + 32 * i] = nl[i];
@@ -244,16 +255,27 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[FULL0 + st]);
+        if (gs >= static_cast<uint32_t>(ST) &&
+            !(ok = mbar_wait_warp(&bars[EMPTYD0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
+          break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[FULLD0 + st], Q_TILE);
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+            tma_load_4d(sq + Q_TILE + s * SLAB, &maps.dO, &bars[FULLD0 + st], s * 64, h, ti.seq_start + q0, ti.b);
+        }
+        pend_d[st] = r & 1;
         if (j + 1 < n) load_rows(j + 1);
-        pend_full[st] = r & 1;
       }
     }
     // loads still in flight land before the CTA exits
     if (lane == 0) {
       if (kv_pend >= 0) mbar_drain(&bars[KV_FULL], kv_pend);
 #pragma unroll
-      for (int i = 0; i < ST; ++i)
+      for (int i = 0; i < ST; ++i) {
         if (pend_full[i] >= 0) mbar_drain(&bars[FULL0 + i], pend_full[i]);
+        if (pend_d[i] >= 0) mbar_drain(&bars[FULLD0 + i], pend_d[i]);
+      }
     }
   } else if (warp == 13) {
     // ============================================================ MMA issuer (whole warp, one elected lane)
@@ -296,7 +318,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           mma_ss_w(tmem + T_S, dK_kmaj + ko, dQ_kmaj + so + ko, IDESC_S, kk > 0);
         }
         mma_commit_w(&bars[S_FULL]);
-        // ---- dP^T: the epilogue has loaded the previous step's dQ from these columns
+        // ---- dP^T: the dO half is loaded and the epilogue has loaded the previous
+        // step's dQ from these columns
+        if (!(ok = mbar_wait_warp(&bars[FULLD0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
         if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DQ_EMPTY], (gs - 1) & 1, wc, kErrWaitDQEmpty))) break;
         tc_fence_after();
 #pragma unroll
@@ -539,11 +563,17 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           lok = mbar_wait(&bars[STG_FULL0 + st], (gs / ST) & 1, wc, kErrWaitStage);
           if (lok) {
             const int c2 = ti.seq_start + q0;
+            // slabs 0-1 lie in the Q half, 2-3 in the dO half: one bulk group each
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
+            for (int s4 = 0; s4 < 2; ++s4) tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
             bulk_commit_group();
-            bulk_wait_read_all();  // the stage may be reloaded once the reduce has read it
+#pragma unroll
+            for (int s4 = 2; s4 < 4; ++s4) tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
+            bulk_commit_group();
+            bulk_wait_read_1();  // the Q half may be reloaded once its reduces have read it
             mbar_arrive(&bars[EMPTY0 + st]);
+            bulk_wait_read_all();
+            mbar_arrive(&bars[EMPTYD0 + st]);
           }
         }
         if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
