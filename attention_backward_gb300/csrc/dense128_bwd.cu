@@ -107,8 +107,9 @@ enum Bar : int {
   DS_SFREE,         // dQ MMAs read the shared dS tile
   DQ_FULL,
   DQ_EMPTY,         // 4 epilogue warps loaded dQ: the dP^T columns are free
-  STG_FULL0,        // ST stages: 4 epilogue warps wrote their staging rows
-  DKV_FULL = STG_FULL0 + ST,
+  STG_FULL0,        // ST stages: 4 epilogue warps wrote their staging rows of the Q half
+  STG_FULLB0 = STG_FULL0 + ST,  // ST stages: ... of the dO half
+  DKV_FULL = STG_FULLB0 + ST,
   DKV_FREE,
   DRAIN,
   NUM_BARS
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       mbar_init(&bars[EMPTY0 + i], 1);
       mbar_init(&bars[EMPTYD0 + i], 1);
       mbar_init(&bars[STG_FULL0 + i], 4);
+      mbar_init(&bars[STG_FULLB0 + i], 4);
     }
     mbar_init(&bars[KV_FULL], 1);
     mbar_init(&bars[KV_FREE], 1);
@@ -534,8 +536,13 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         // dQ complete (so dV and dK, issued before it, have read this step's stage)
         if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
-        // f32 staging in the stage: four 128-byte-swizzled slabs [128 queries x 32 d]
+        // f32 staging in the stage: four 128-byte-swizzled slabs [128 queries x 32 d],
+        // d 0-63 (slabs 0-1) in the Q half and d 64-127 (slabs 2-3) in the dO half.
+        // Each half is written, then added with two reduces as one bulk group, so
+        // the Q half's reduces start before the dO half is staged.
         uint8_t* stg = sm + OFF_STAGE + st * STAGE;
+        const int c2 = ti.seq_start + q0;
+        bool lok = true;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[64];
@@ -554,27 +561,27 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
                 make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
                             __uint_as_float(r[4 * c + 3]));
           }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[STG_FULL0 + st]);
-        bool lok = true;
-        if (leader) {
-          lok = mbar_wait(&bars[STG_FULL0 + st], (gs / ST) & 1, wc, kErrWaitStage);
-          if (lok) {
-            const int c2 = ti.seq_start + q0;
-            // slabs 0-1 lie in the Q half, 2-3 in the dO half: one bulk group each
+          fence_proxy_async_smem();
+          __syncwarp();
+          uint64_t* full = &bars[(hf == 0 ? STG_FULL0 : STG_FULLB0) + st];
+          if (lane == 0) mbar_arrive(full);
+          if (leader && lok) {
+            lok = mbar_wait(full, (gs / ST) & 1, wc, kErrWaitStage);
+            if (lok) {
 #pragma unroll
-            for (int s4 = 0; s4 < 2; ++s4) tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
-            bulk_commit_group();
-#pragma unroll
-            for (int s4 = 2; s4 < 4; ++s4) tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
-            bulk_commit_group();
-            bulk_wait_read_1();  // the Q half may be reloaded once its reduces have read it
-            mbar_arrive(&bars[EMPTY0 + st]);
-            bulk_wait_read_all();
-            mbar_arrive(&bars[EMPTYD0 + st]);
+              for (int s2 = 0; s2 < 2; ++s2) {
+                const int s4 = 2 * hf + s2;
+                tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
+              }
+              bulk_commit_group();
+            }
           }
+        }
+        if (leader && lok) {
+          bulk_wait_read_1();  // the Q half may be reloaded once its reduces have read it
+          mbar_arrive(&bars[EMPTY0 + st]);
+          bulk_wait_read_all();
+          mbar_arrive(&bars[EMPTYD0 + st]);
         }
         if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
       }
