@@ -34,9 +34,10 @@
 // go back to the producer separately, each as soon as the reduces of its own
 // two staging slabs have read it.
 //
-// Warp roles (14 warps): 0-3 dQ epilogue (lane = query), 4-11 two warpgroups
-// of softmax/dS work (each owns 64 of the 128 query columns of all 128 key
-// rows) that also land dK/dV, 12 TMA producer, 13 MMA issuer.  A stage, a
+// Warp roles (14 warps): 0-3 dQ epilogue (lane = query; at the end of a tile
+// they also land dK/dV, lane = key row, while the softmax warps start the next
+// one), 4-11 two warpgroups of softmax/dS work (each owns 64 of the 128 query
+// columns of all 128 key rows), 12 TMA producer, 13 MMA issuer.  A stage, a
 // TMEM region or the dS tile is reused only after an mbarrier shows that its
 // last reader is done.  Every wait is bounded.
 #include <cuda_bf16.h>
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     mbar_init(&bars[DQ_FULL], 1);
     mbar_init(&bars[DQ_EMPTY], 4);
     mbar_init(&bars[DKV_FULL], 1);
-    mbar_init(&bars[DKV_FREE], 8);
+    mbar_init(&bars[DKV_FREE], 4);  // the 4 dQ epilogue warps land dK/dV
     mbar_init(&bars[DRAIN], 1);
     fence_mbar_init();
   }
@@ -477,42 +478,6 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (lane == 0) mbar_arrive(&bars[DS_READY]);
       }
       if (!ok) break;
-      // ---- dK / dV of the tile: warpgroup 0 lands dV, warpgroup 1 lands dK (times sm_scale)
-      if (!(ok = mbar_wait_warp(&bars[DKV_FULL], tc & 1, wc, kErrWaitDKV))) break;
-      tc_fence_after();
-      const bool isK = wg == 1;
-      const uint32_t col0 = isK ? T_DK : T_DV;
-      const float mul = isK ? p.sm_scale : 1.f;
-      const int64_t pos = ti.seq_start + kpos;
-      uint8_t* out = isK ? p.dk + 2 * (ti.b * p.sdk_b + pos * p.sdk_s + ti.g * p.sdk_h)
-                         : p.dv + 2 * (ti.b * p.sdv_b + pos * p.sdv_s + ti.g * p.sdv_h);
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        if (n > 0) {
-          tmem_ld32(tmem + lane_off + col0 + ch * 32, r);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = 0u;
-        }
-        if (ch == D / 32 - 1) {  // the accumulators may be overwritten by the next tile from here on
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[DKV_FREE]);
-        }
-        if (kvalid) {
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint4 v;
-            v.x = pack2<BF16>(__uint_as_float(r[c8 * 8 + 0]) * mul, __uint_as_float(r[c8 * 8 + 1]) * mul);
-            v.y = pack2<BF16>(__uint_as_float(r[c8 * 8 + 2]) * mul, __uint_as_float(r[c8 * 8 + 3]) * mul);
-            v.z = pack2<BF16>(__uint_as_float(r[c8 * 8 + 4]) * mul, __uint_as_float(r[c8 * 8 + 5]) * mul);
-            v.w = pack2<BF16>(__uint_as_float(r[c8 * 8 + 6]) * mul, __uint_as_float(r[c8 * 8 + 7]) * mul);
-            *reinterpret_cast<uint4*>(out + 2 * (ch * 32 + c8 * 8)) = v;
-          }
-        }
-      }
     }
   } else {
     // ============================================================ dQ epilogue (lane = query)
@@ -584,6 +549,50 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           mbar_arrive(&bars[EMPTYD0 + st]);
         }
         if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
+      }
+      if (!ok) break;
+      // ---- dK / dV of the tile, once every MMA of the tile has completed: lane =
+      // key row, dV then dK (times sm_scale) in 32-column chunks.  The softmax
+      // warps meanwhile start the next tile, whose first dV MMA waits for
+      // DKV_FREE (all chunks loaded from TMEM).
+      if (!(ok = mbar_wait_warp(&bars[DKV_FULL], tc & 1, wc, kErrWaitDKV))) break;
+      tc_fence_after();
+      const int kpos = ti.k0 + q;
+      const bool kvalid = kpos < ti.len;
+      const int64_t pos = ti.seq_start + kpos;
+      uint8_t* const out_v = p.dv + 2 * (ti.b * p.sdv_b + pos * p.sdv_s + ti.g * p.sdv_h);
+      uint8_t* const out_k = p.dk + 2 * (ti.b * p.sdk_b + pos * p.sdk_s + ti.g * p.sdk_h);
+      constexpr int NCK = D / 32;  // chunks per accumulator
+#pragma unroll 1
+      for (int cc = 0; cc < 2 * NCK; ++cc) {
+        const bool isK = cc >= NCK;
+        const int ch = isK ? cc - NCK : cc;
+        const float mul = isK ? p.sm_scale : 1.f;
+        uint8_t* const out = isK ? out_k : out_v;
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_off + (isK ? T_DK : T_DV) + ch * 32, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
+        if (cc == 2 * NCK - 1) {  // the accumulators may be overwritten by the next tile from here on
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[DKV_FREE]);
+        }
+        if (kvalid) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 v;
+            v.x = pack2<BF16>(__uint_as_float(r[c8 * 8 + 0]) * mul, __uint_as_float(r[c8 * 8 + 1]) * mul);
+            v.y = pack2<BF16>(__uint_as_float(r[c8 * 8 + 2]) * mul, __uint_as_float(r[c8 * 8 + 3]) * mul);
+            v.z = pack2<BF16>(__uint_as_float(r[c8 * 8 + 4]) * mul, __uint_as_float(r[c8 * 8 + 5]) * mul);
+            v.w = pack2<BF16>(__uint_as_float(r[c8 * 8 + 6]) * mul, __uint_as_float(r[c8 * 8 + 7]) * mul);
+            *reinterpret_cast<uint4*>(out + 2 * (ch * 32 + c8 * 8)) = v;
+          }
+        }
       }
     }
     if (leader) bulk_wait_all();
