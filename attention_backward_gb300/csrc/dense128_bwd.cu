@@ -57,7 +57,10 @@ constexpr int D = 128;
 constexpr int BM = kDenseBM;
 constexpr int BN = 128;
 constexpr int ST = 2;                 // Q/dO stages
-constexpr int PREFETCH = 4;           // L2 prefetch distance of Q/dO/LSE/delta, in steps
+// L2 prefetch distance of Q/dO/LSE/delta, in steps.  Long tiles (unmasked GQA)
+// gain from it; the short tiles of causal launches (at most 16 steps at S =
+// 2048) run faster without prefetches, which this distance leaves out.
+constexpr int PREFETCH = 32;
 constexpr int SLAB = 128 * 128;       // [128 rows x 64 cols] 16-bit, 128-byte swizzled
 constexpr int KV_TILE = 2 * SLAB;     // 128 rows x 128 cols
 constexpr int Q_TILE = 2 * SLAB;

@@ -21,7 +21,7 @@ __host__ __device__ constexpr uint32_t pair_col(int q, int half) {
 }
 
 // (batch, KV head) pairs whose tiles are drawn together (dense batches).
-constexpr int kTileGroup = 16;
+constexpr int kTileGroup = 8;
 
 // Tile t -> (batch, KV head, key block); longest tiles first (smallest key
 // block index first, which is the longest under a causal mask).  Dense
