@@ -208,15 +208,14 @@ attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn
   }
   const WsLayout L = ws_layout(B, S, HQ, D, 0);
   if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
-  const int BN = dense_launch_bn(static_cast<int>(D), causal != 0 || window > 0);
+  const int BN = kDenseBN;
   DenseMaps m;
   if (!make_map(&m.q, q, dtype, B, S, HQ, D, sq, BN) || !make_map(&m.dO, dO, dtype, B, S, HQ, D, sdo, BN) ||
       !make_map(&m.k, k, dtype, B, S, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, S, HKV, D, sv, kDenseBM))
     return ATTN_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // dQ partials: 64-query steps of head dim 128 land [64 x 128 d] boxes, 128-query
-  // steps land [128 x 32 d] boxes staged with a 128-byte swizzle
-  if (!make_acc_map(&m.dq, ws + L.dq_off, B, S, HQ, D, BN == 64 ? 128 : 32, BN)) return ATTN_ERR_INVALID_ARG;
+  // dQ partials land as [128 queries x 32 d] boxes staged with a 128-byte swizzle
+  if (!make_acc_map(&m.dq, ws + L.dq_off, B, S, HQ, D, 32, BN)) return ATTN_ERR_INVALID_ARG;
   DenseParams p{};
   p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV);
   p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D);

@@ -19,16 +19,19 @@
 //   dQ   = dS K                    from shared memory; added into the f32 workspace
 //                                  accumulator with one bulk tensor reduce-add
 //
-// D = 128 uses BN = 64 and computes dQ^T = K^T dS^T (M = 128 head dims);
-// D = 64 uses BN = 128 and computes dQ = dS K (M = 128 queries).
+// This kernel serves head dim 64 with BN = 128 queries per step and computes
+// dQ = dS K (M = 128 queries); head dim 128 runs the kernel of
+// dense128_bwd.cu.
 //
 // Pipelining: S^T is double-buffered in TMEM and the S^T of step i+1 is
 // issued before dV/dK/dQ of step i, so the softmax of one step overlaps the
 // tensor work of the previous one.  P^T and dS^T of a step are written over
-// that step's S^T columns.  Q/dO come through a 3-stage TMA ring.  A stage is
-// released only by a tensor-core commit issued after every MMA reading it,
-// and no accumulator is read before its commit completed (the two pipelining
-// faults the TileOPs page reports fixing in its older kernel, "Summary").
+// that step's S^T columns, and its dQ goes there once dK has read them.
+// Q/dO come through a 3-stage TMA ring; the f32 dQ partial of a step is
+// staged in the step's own stage and the stage goes back to the producer once
+// the dQ reduces have read it.  No stage or accumulator is reused before an
+// mbarrier shows that its last reader is done (the two pipelining faults the
+// TileOPs page reports fixing in its older kernel, "Summary").
 //
 // Persistent CTAs (one per SM) draw tiles, longest first, from a counter in
 // the workspace that the preprocess zeroes; each CTA's producer publishes the
@@ -37,7 +40,7 @@
 // Warp roles (14 warps): 0-3 dQ epilogue (TMEM -> shared -> bulk reduce),
 // 4-11 two warpgroups of softmax/dS work (each owns half of the BN query
 // columns of all 128 key rows) that also land dK/dV, 12 TMA producer,
-// 13 MMA issuer (one thread).  Every wait is bounded.
+// 13 MMA issuer (one elected thread).  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -53,14 +56,11 @@ namespace {
 
 template <int D>
 struct Cfg {
+  static_assert(D == 64, "head dim 128 runs the kernel of dense128_bwd.cu");
   static constexpr int BM = kDenseBM;
-  static constexpr int BN = dense_bn(D);
-  // Head dim 64 stages the f32 dQ partial of a step in the step's own Q/dO
-  // stage once its MMAs are done, which leaves room for a second dS tile.
-  // Head dim 128 keeps a separate staging buffer: there the stage would be
-  // released later than the dK MMA releases it, which was measured slower
-  // even with a fourth stage in the freed space.
-  static constexpr bool STG_IN_STAGE = D == 64;
+  static constexpr int BN = kDenseBN;
+  // The f32 dQ partial of a step is staged in the step's own Q/dO stage once
+  // its MMAs are done, which leaves room for a second dS tile.
   static constexpr int STAGES = 3;  // the barrier layout below holds up to 3
   static constexpr int PREFETCH = 8;  // L2 prefetch distance of Q/dO/LSE/delta, in steps
   static constexpr int NSLAB = D / 64;  // 64-column (128-byte) slabs per row
@@ -70,7 +70,6 @@ struct Cfg {
   static constexpr int Q_TILE = Q_SLAB * NSLAB;
   static constexpr int DS_BYTES = BM * BN * 2;
   static constexpr int NDS = 2;  // dS tiles in shared memory (double-buffered)
-  static constexpr int STG_BYTES = STG_IN_STAGE ? 0 : BN * D * 4;  // separate f32 dQ staging
   static_assert(BN * D * 4 == 2 * Q_TILE, "the f32 dQ staging of a step fills a Q/dO stage");
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
@@ -78,8 +77,7 @@ struct Cfg {
   static constexpr int OFF_Q = OFF_V + KV_TILE;
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_TILE;
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
-  static constexpr int OFF_STG = OFF_DS + NDS * DS_BYTES;
-  static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
+  static constexpr int OFF_LSE = OFF_DS + NDS * DS_BYTES;
   static constexpr int OFF_DELTA = OFF_LSE + STAGES * BN * 4;
   static constexpr int OFF_RING = OFF_DELTA + STAGES * BN * 4;
   static constexpr int OFF_BAR = OFF_RING + 64;
@@ -93,10 +91,9 @@ struct Cfg {
   static constexpr int T_DP = 2 * BN;      // dP^T f32 [128 x BN]
   static constexpr int T_DV = 3 * BN;      // dV f32 [128 x D]
   static constexpr int T_DK = 3 * BN + D;  // dK f32 [128 x D]
-  // dQ^T [128 d x 64 q] in its own columns (D = 128); for D = 64, dQ [128 q x 64 d]
-  // goes into the first 64 columns of its step's S^T buffer once dK has read that buffer
-  static constexpr int T_DQ = 3 * BN + 2 * D;
-  static_assert(3 * BN + 2 * D + (D == 128 ? 64 : 0) <= 512, "TMEM budget");
+  // dQ [128 q x 64 d] goes into the first 64 columns of its step's S^T buffer
+  // once dK has read that buffer
+  static_assert(3 * BN + 2 * D <= 512, "TMEM budget");
   static constexpr int THREADS = 14 * 32;
 };
 
@@ -108,15 +105,13 @@ enum Bar : int {
   TILE_FULL0 = 8,   // 2 slots
   TILE_EMPTY0 = 10, // 2 slots
   S_FULL0 = 12,     // 2 buffers
-  S_FREE0 = 14,     // 2 buffers
-  P_READY0 = 16,    // 2 buffers
-  DP_FULL = 18,
+  P_READY0 = 14,    // 2 buffers
+  DP_FULL = 16,
   DS_READY,
   DS_SFREE0,        // 2 dS tiles
   DQ_FULL = DS_SFREE0 + 2,
   DQ_EMPTY,
   STG_FULL,         // 4 epilogue warps wrote their staging rows
-  STG_FREE,         // the separate staging buffer has been read by the previous reduce
   DKV_FULL,
   DKV_FREE,
   DRAIN,
@@ -156,7 +151,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       mbar_init(&bars[TILE_FULL0 + i], 1);
       mbar_init(&bars[TILE_EMPTY0 + i], 13);  // MMA thread + 8 compute warps + 4 epilogue warps
       mbar_init(&bars[S_FULL0 + i], 1);
-      mbar_init(&bars[S_FREE0 + i], 1);
     }
     mbar_init(&bars[P_READY0], 8);
     mbar_init(&bars[P_READY0 + 1], 8);
@@ -167,7 +161,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[DQ_FULL], 1);
     mbar_init(&bars[DQ_EMPTY], 4);
     mbar_init(&bars[STG_FULL], 4);
-    mbar_init(&bars[STG_FREE], 1);
     mbar_init(&bars[DKV_FULL], 1);
     mbar_init(&bars[DKV_FREE], 8);
     mbar_init(&bars[DRAIN], 1);
@@ -324,14 +317,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           // ---- S^T of step nxt into buffer nxt & 1
           const int st = nxt % ST;
           if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (nxt / ST) & 1, wc, kErrWaitStageFull))) break;
-          if (nxt >= 2) {
-            // the buffer's previous readers: dV/dK of step nxt-2 (D = 128), or the
-            // epilogue's readout of the dQ that overwrote it (D = 64; readouts are
-            // in step order, so the latest issued dQ is waited for)
-            ok = D == 128 ? mbar_wait_warp(&bars[S_FREE0 + (nxt & 1)], ((nxt - 2) >> 1) & 1, wc, kErrWaitSFree)
-                          : mbar_wait_warp(&bars[DQ_EMPTY], static_cast<uint32_t>(last_dq) & 1, wc, kErrWaitDQEmpty);
-            if (!ok) break;
-          }
+          // the buffer's last reader is the epilogue's readout of the dQ that
+          // overwrote it (readouts are in step order, so the latest issued dQ is
+          // waited for)
+          if (nxt >= 2 &&
+              !(ok = mbar_wait_warp(&bars[DQ_EMPTY], static_cast<uint32_t>(last_dq) & 1, wc, kErrWaitDQEmpty)))
+            break;
           tc_fence_after();
           const uint32_t dS_acc = tmem + C::T_SB + (nxt & 1) * BN;
           const uint64_t qo = sdesc_step(st * C::Q_TILE);
@@ -389,31 +380,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_w(tmem + C::T_DK, sb + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + qo + sdesc_step(kk * 2048),
                    IDESC_KV, j > 0 || kk > 0);
-        // with a separate staging buffer, the dK MMA is the last reader of the stage
-        if constexpr (!C::STG_IN_STAGE) mma_commit_w(&bars[EMPTY0 + st]);
-        uint32_t dq_cols;
-        if constexpr (D == 128) {
-          mma_commit_w(&bars[S_FREE0 + (cur & 1)]);  // P^T / dS^T of this buffer consumed
-          dq_cols = tmem + C::T_DQ;
-        } else {
-          // dQ overwrites this step's S^T buffer: dV and dK must have read it
-          mma_commit_w(&bars[DK_DONE]);
-          if (!(ok = mbar_wait_warp(&bars[DK_DONE], cur & 1, wc, kErrWaitSFree))) break;
-          dq_cols = sb;
-        }
+        // dQ overwrites this step's S^T buffer: dV and dK must have read it
+        mma_commit_w(&bars[DK_DONE]);
+        if (!(ok = mbar_wait_warp(&bars[DK_DONE], cur & 1, wc, kErrWaitSFree))) break;
+        const uint32_t dq_cols = sb;
         // one dQ in flight: the epilogue has read the previous one
         if (cur >= 1 && !(ok = mbar_wait_warp(&bars[DQ_EMPTY], (cur - 1) & 1, wc, kErrWaitDQEmpty))) break;
         tc_fence_after();
         // ---- dQ over the 128 key rows (K-step = 16 key rows = 2048 bytes)
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          if constexpr (D == 128)  // dQ^T = K^T dS^T: A = K tile MN-major, B = dS^T MN-major
-            mma_ss_w(dq_cols, dK_mn + sdesc_step(kk * 2048),
-                     dDS_mn + sdesc_step((cur % C::NDS) * C::DS_BYTES + kk * 2048), IDESC_DQ, kk > 0);
-          else  // dQ = dS K: A = dS MN-major (two 64-query blocks), B = K tile MN-major
-            mma_ss_w(dq_cols, dDS_mn + sdesc_step((cur % C::NDS) * C::DS_BYTES + kk * 2048),
-                     dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
-        }
+        for (int kk = 0; kk < BM / 16; ++kk)  // A = dS MN-major (two 64-query blocks), B = K tile MN-major
+          mma_ss_w(dq_cols, dDS_mn + sdesc_step((cur % C::NDS) * C::DS_BYTES + kk * 2048),
+                   dK_mn + sdesc_step(kk * 2048), IDESC_DQ, kk > 0);
         mma_commit_w(&bars[DQ_FULL]);
         mma_commit_w(&bars[DS_SFREE0 + cur % C::NDS]);
         last_dq = cur;
@@ -467,54 +445,29 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
           tmem_ld32(sb + wg * HALF + ch * 32, r);
-          if constexpr (NCH == 1) {
-            // one chunk per thread: LSE2 is read while the TMEM load is in flight
-            float lse[32];
+          tmem_ld_wait();
+          // LSE2 four columns at a time, so that only r and pv stay live
+          if (full_vis) {
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
               const float4 t = lse4[ch * 8 + c4];
-              lse[4 * c4] = t.x, lse[4 * c4 + 1] = t.y, lse[4 * c4 + 2] = t.z, lse[4 * c4 + 3] = t.w;
+              const float l4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                pv[ch * 32 + 4 * c4 + e] = ex2(fmaf(__uint_as_float(r[4 * c4 + e]), p.scale_log2, -l4[e]));
             }
-            tmem_ld_wait();
-            if (full_vis) {
+          } else {
 #pragma unroll
-              for (int c = 0; c < 32; ++c)
-                pv[ch * 32 + c] = ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c]));
-            } else {
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 t = lse4[ch * 8 + c4];
+              const float l4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const int cc = ch * 32 + c, q = qc0 + cc;
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * c4 + e, cc = ch * 32 + c, q = qc0 + cc;
                 bool vis = kvalid && q < ti.len;
                 if (cm) vis = vis && kpos <= q;
                 if (W > 0) vis = vis && q < kpos + W;
-                pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -lse[c])) : 0.f;
-              }
-            }
-          } else {
-            tmem_ld_wait();
-            // LSE2 four columns at a time, so that only r and pv stay live
-            if (full_vis) {
-  #pragma unroll
-              for (int c4 = 0; c4 < 8; ++c4) {
-                const float4 t = lse4[ch * 8 + c4];
-                const float l4[4] = {t.x, t.y, t.z, t.w};
-  #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  pv[ch * 32 + 4 * c4 + e] = ex2(fmaf(__uint_as_float(r[4 * c4 + e]), p.scale_log2, -l4[e]));
-              }
-            } else {
-  #pragma unroll
-              for (int c4 = 0; c4 < 8; ++c4) {
-                const float4 t = lse4[ch * 8 + c4];
-                const float l4[4] = {t.x, t.y, t.z, t.w};
-  #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int c = 4 * c4 + e, cc = ch * 32 + c, q = qc0 + cc;
-                  bool vis = kvalid && q < ti.len;
-                  if (cm) vis = vis && kpos <= q;
-                  if (W > 0) vis = vis && q < kpos + W;
-                  pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -l4[e])) : 0.f;
-                }
+                pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -l4[e])) : 0.f;
               }
             }
           }
@@ -535,11 +488,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
 
         if (!(ok = mbar_wait_warp(&bars[DP_FULL], gs & 1, wc, kErrWaitDP))) break;
         // the dS tile this step writes was last read by the dQ of step gs - NDS
-        auto ds_tile_free = [&]() -> bool {
-          return gs < static_cast<uint32_t>(C::NDS) ||
-                 mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree);
-        };
-        if (NCH > 1 && !(ok = ds_tile_free())) break;
+        if (gs >= static_cast<uint32_t>(C::NDS) &&
+            !(ok = mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree)))
+          break;
         tc_fence_after();
         // each 32-query chunk of dS is stored as soon as it is computed, so only
         // one chunk of packed pairs is live next to P
@@ -567,28 +518,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[c + 1]);
             dsw[c / 2] = pack2<BF16>(d0, d1);
           }
-          if (NCH == 1) {
-            if (!(ok = ds_tile_free())) break;
-            tc_fence_after();
-          }
           // dS^T pairs into the second half of this warpgroup's S^T columns
           tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
-          if constexpr (D == 128) {
-            // dS^T as the MN-major B operand [128 key rows x 64 queries]: my 32
-            // queries are 16-byte chunks 4*wg .. 4*wg+3 of row ``row``
-            uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES;
+          // dS as the MN-major A operand of dQ: 64-query block wg, row = key, chunks 4ch .. 4ch+3
+          uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES + wg * (BM * 128);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-              *reinterpret_cast<uint4*>(base + sw128_offset(row, wg * 4 + c4)) =
-                  make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
-          } else {
-            // dS as the MN-major A operand: 64-query block wg, row = key, chunks 4ch .. 4ch+3
-            uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES + wg * (BM * 128);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-              *reinterpret_cast<uint4*>(base + sw128_offset(row, ch * 4 + c4)) =
-                  make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
-          }
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(base + sw128_offset(row, ch * 4 + c4)) =
+                make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
         }
         if (!ok) break;
         fence_proxy_async_smem();
@@ -637,13 +574,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     }
   } else {
     // ============================================================ dQ epilogue
-    // Head dim 64: the f32 dQ partial of a step is staged in the step's own
-    // Q/dO stage (every MMA reading the stage was issued before dQ, so it has
-    // completed once DQ_FULL has), one 128-byte-swizzled [128 q x 32 d] slab in
-    // the Q part and one in the dO part, and the stage is handed back to the
-    // producer once the two bulk tensor reduce-adds have read it.  Head dim 128:
-    // staged as [64 q x 128 d] in the separate buffer, which is reused once the
-    // previous reduce has read it.
+    // The f32 dQ partial of a step is staged in the step's own Q/dO stage (every
+    // MMA reading the stage was issued before dQ, so it has completed once
+    // DQ_FULL has), one 128-byte-swizzled [128 q x 32 d] slab in the Q part and
+    // one in the dO part, and the stage is handed back to the producer once the
+    // two bulk tensor reduce-adds have read it.
     const int quad = warp;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool leader = warp == 0 && lane == 0;
@@ -664,7 +599,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
         uint32_t r[64];
-        const uint32_t dq_cols = tmem + lane_off + (D == 128 ? C::T_DQ : C::T_SB + (gs & 1u) * BN);
+        const uint32_t dq_cols = tmem + lane_off + C::T_SB + (gs & 1u) * BN;
         tmem_ld32(dq_cols, r);
         tmem_ld32(dq_cols + 32, r + 32);
         tmem_ld_wait();
@@ -673,28 +608,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         if (lane == 0) mbar_arrive(&bars[DQ_EMPTY]);
         uint8_t* const half0 = sm + C::OFF_Q + st * C::Q_TILE;
         uint8_t* const half1 = sm + C::OFF_DO + st * C::Q_TILE;
-        float* const stg = reinterpret_cast<float*>(sm + C::OFF_STG);
-        if constexpr (C::STG_IN_STAGE) {
-          // lane = query; half c / 8 is a 128-byte-swizzled slab [128 q][32 d]
-          const int q = quad * 32 + lane;
+        // lane = query; half c / 8 is a 128-byte-swizzled slab [128 q][32 d]
+        const int q = quad * 32 + lane;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            uint8_t* slab = c < 8 ? half0 : half1;
-            *reinterpret_cast<float4*>(slab + sw128_offset(q, c & 7)) =
-                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
-                            __uint_as_float(r[4 * c + 3]));
-          }
-        } else {
-          // the separate staging buffer is free once the previous reduce has read it
-          if (leader) {
-            if (issued) bulk_wait_read_all();
-            mbar_arrive(&bars[STG_FREE]);
-          }
-          if (!(ok = mbar_wait_warp(&bars[STG_FREE], gs & 1, wc, kErrWaitStage))) break;
-          // lane = head dim d; staging [64 queries][128 d] f32, rows of 512 bytes
-          const int d = quad * 32 + lane;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) stg[c * 128 + d] = __uint_as_float(r[c]);
+        for (int c = 0; c < 16; ++c) {
+          uint8_t* slab = c < 8 ? half0 : half1;
+          *reinterpret_cast<float4*>(slab + sw128_offset(q, c & 7)) =
+              make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
+                          __uint_as_float(r[4 * c + 3]));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -704,16 +625,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           lok = mbar_wait(&bars[STG_FULL], gs & 1, wc, kErrWaitStage);
           if (lok) {
             const int c2 = ti.seq_start + q0;
-            if constexpr (C::STG_IN_STAGE) {
-              tma_reduce_add_4d(&maps.dq, half0, 0, h, c2, ti.b);
-              tma_reduce_add_4d(&maps.dq, half1, D / 2, h, c2, ti.b);
-              bulk_commit_group();
-              bulk_wait_read_all();  // the stage may be reloaded once the reduces have read it
-              mbar_arrive(&bars[EMPTY0 + st]);
-            } else {
-              tma_reduce_add_4d(&maps.dq, stg, 0, h, c2, ti.b);
-              bulk_commit_group();
-            }
+            tma_reduce_add_4d(&maps.dq, half0, 0, h, c2, ti.b);
+            tma_reduce_add_4d(&maps.dq, half1, D / 2, h, c2, ti.b);
+            bulk_commit_group();
+            bulk_wait_read_all();  // the stage may be reloaded once the reduces have read it
+            mbar_arrive(&bars[EMPTY0 + st]);
             issued = true;
           }
         }
@@ -760,9 +676,9 @@ __global__ void selftest_timeout_kernel(int* err, uint64_t timeout_ns) {
 }  // namespace
 
 cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st) {
-  if (p.D == 128 && p.bn == 128) return launch_dense128(p, m, bf16, grid, st);
-  if (p.bn != dense_bn(p.D)) return cudaErrorInvalidValue;
-  if (p.D == 128) return bf16 ? launch_dense_t<128, true>(p, m, grid, st) : launch_dense_t<128, false>(p, m, grid, st);
+  if (p.bn != kDenseBN) return cudaErrorInvalidValue;
+  if (p.D == 128) return launch_dense128(p, m, bf16, grid, st);
+  if (p.D != 64) return cudaErrorInvalidValue;
   return bf16 ? launch_dense_t<64, true>(p, m, grid, st) : launch_dense_t<64, false>(p, m, grid, st);
 }
 

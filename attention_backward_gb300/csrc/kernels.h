@@ -88,23 +88,15 @@ cudaError_t launch_sparse(const SparseParams& p, const SparseMaps& m, bool bf16,
 cudaError_t launch_preprocess(const PreprocessParams& p, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_land(const LandParams& p, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);
-// Head dim 128 with 128-query steps (dense128_bwd.cu); launch_dense forwards
-// launches with p.bn == 128 and p.D == 128 here.
+// Head dim 128 (dense128_bwd.cu); launch_dense forwards launches with
+// p.D == 128 here and runs head dim 64 itself (dense_bwd.cu).
 cudaError_t launch_dense128(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_selftest_timeout(int* err, uint64_t timeout_ns, cudaStream_t st);
 
-// Block sizes of the dense kernel (keys per tile, queries per step).
+// Block sizes of both dense kernels: keys per tile, and queries per step
+// (every MMA at N = 128; 64-query steps with a double-buffered S^T measured
+// slower at head dim 128 on both the causal and the unmasked workloads).
 constexpr int kDenseBM = 128;
-// Query rows per step of the key-block kernel of dense_bwd.cu (64 for head dim
-// 128, whose double-buffered S^T then fits tensor memory; 128 for head dim 64).
-__host__ __device__ constexpr int dense_bn(int D) { return D == 128 ? 64 : 128; }
-// Query rows per step of a dense launch: head dim 128 runs the 128-query
-// kernel of dense128_bwd.cu (every MMA at N = 128; measured faster than the
-// 64-query steps of dense_bwd.cu on both the causal and the unmasked
-// workloads), head dim 64 the kernel of dense_bwd.cu.
-inline int dense_launch_bn(int D, bool masked) {
-  (void)masked;
-  return D == 128 ? 128 : dense_bn(D);
-}
+constexpr int kDenseBN = 128;
 
 }  // namespace ab
