@@ -22,5 +22,6 @@ from ._binding import (  # noqa: F401
     selftest_timeout,
     sparse_backward,
     sparse_land,
+    tile_schedule,
     workspace_size,
 )

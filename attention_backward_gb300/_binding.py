@@ -50,6 +50,8 @@ _SIGS = {
     "attn_bwd_status_string": (ctypes.c_char_p, [c_i32]),
     "attn_bwd_query_block_range": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                           ctypes.POINTER(c_i32)]),
+    "attn_bwd_tile_schedule": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32), c_i32,
+                                      ctypes.POINTER(c_i32)]),
     "attn_bwd_selftest_timeout": (c_i32, [c_vp, c_sz, c_i32, c_vp]),
     "attn_bwd_gqa_noalloc": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides,
                                      c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32,
@@ -226,6 +228,19 @@ def query_block_range(k0: int, block_k: int, length: int, causal: bool, window: 
     library().attn_bwd_query_block_range(k0, block_k, length, int(causal), int(window), block_q, ctypes.byref(lo),
                                          ctypes.byref(hi))
     return lo.value, hi.value
+
+
+def tile_schedule(t: int, B: int, S: int, HKV: int, causal: bool, window: int, cu_seqlens=None) -> tuple:
+    """The dense kernels' t-th tile draw: (valid, b, kv head, sequence start,
+    first key, first query block, number of query blocks)."""
+    out = (c_i32 * 7)()
+    cu = None
+    n = 0
+    if cu_seqlens is not None:
+        n = len(cu_seqlens) - 1
+        cu = (c_i32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
+    library().attn_bwd_tile_schedule(t, B, S, HKV, int(causal), int(window), cu, n, out)
+    return tuple(out)
 
 
 def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1,

@@ -11,6 +11,7 @@
 
 #include "attn_bwd.h"
 #include "common.cuh"
+#include "dense_common.cuh"
 #include "kernels.h"
 
 namespace {
@@ -145,6 +146,22 @@ void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_t len, int32_
   if (block_k > 0 && block_q > 0) query_block_range(k0, block_k, len, causal, window_left, block_q, &l, &h);
   if (lo) *lo = l;
   if (hi) *hi = h;
+}
+
+void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t causal, int32_t window_left,
+                            const int32_t* cu_seqlens, int32_t num_seqs, int32_t* out) {
+  if (!out) return;
+  TileInfo ti{};
+  if (B >= 1 && S >= 1 && HKV >= 1 && (!cu_seqlens || num_seqs >= 1)) {
+    DenseParams p{};
+    p.B = B, p.S = S, p.HKV = HKV;
+    p.causal = causal ? 1 : 0, p.window = window_left;
+    p.cu_seqlens = cu_seqlens, p.num_seqs = cu_seqlens ? num_seqs : 0;
+    p.bn = kDenseBN;
+    ti = decode_tile(t, p);
+  }
+  const int32_t v[7] = {ti.valid, ti.b, ti.g, ti.seq_start, ti.k0, ti.qlo, ti.nq};
+  for (int i = 0; i < 7; ++i) out[i] = ti.valid ? v[i] : 0;
 }
 
 attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,

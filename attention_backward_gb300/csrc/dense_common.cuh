@@ -31,7 +31,8 @@ constexpr int kTileGroup = 8;
 // load balance (each group still ends with its shortest tiles).  Packed
 // sequences keep key block major order over all pairs (their tile count per
 // pair is known only on the device, and the draws past it end a CTA's work).
-static __device__ __forceinline__ TileInfo decode_tile(int t, const DenseParams& p) {
+// Host code may call it too (with cu_seqlens in host memory) to check the order.
+static __host__ __device__ __forceinline__ TileInfo decode_tile(int t, const DenseParams& p) {
   TileInfo ti{};
   ti.valid = 0;
   const int BH = p.B * p.HKV;

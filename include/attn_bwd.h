@@ -189,6 +189,21 @@ ATTN_BWD_API const char* attn_bwd_status_string(attn_status_t status);
 ATTN_BWD_API void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_t len, int32_t causal, int32_t window_left,
                                 int32_t block_q, int32_t* lo, int32_t* hi);
 
+/* Host-side schedule helper, exported so that the persistent tile order of the
+ * dense kernels can be checked on the host.  Tile ``t`` is the t-th draw from
+ * the tile counter of a launch over B batch rows, S positions and HKV KV heads
+ * with the mask (causal, window_left) and, for packed sequences, cu_seqlens
+ * (HOST memory here, [num_seqs + 1]; NULL for dense batches).  Tiles are 128
+ * keys, query blocks 128 rows; dense batches go through the (batch, KV head)
+ * pairs in groups of 8, key block major inside a group (the longest tiles of a
+ * group first under a causal mask), packed sequences key block major over all
+ * pairs.  Writes out[0..6] = {valid, b, kv head, sequence start, first key
+ * (sequence-local), first query block, number of query blocks}; valid = 0 for
+ * a draw past the last tile or invalid sizes (B, S, HKV < 1). */
+ATTN_BWD_API void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t causal,
+                                         int32_t window_left, const int32_t* cu_seqlens, int32_t num_seqs,
+                                         int32_t* out);
+
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on a
  * barrier nothing signals, with a ``timeout_us`` limit, and returns what
  * attn_bwd_check_error then reports (ATTN_ERR_TIMEOUT when the machinery

@@ -77,6 +77,50 @@ def test_causal_step_count_matches_the_page(ab):
     assert steps == 272
 
 
+def _host_tile_bound(B, S, HKV, cu):
+    """Tile draws the host sizes a launch for: 128-key tiles per (batch, KV
+    head), one extra partial tile per packed sequence."""
+    return ((S + 127) // 128 + (len(cu) - 1 if cu else 0)) * B * HKV
+
+
+@pytest.mark.parametrize("B,S,HKV,causal,window,cu", [
+    (2, 2048, 32, True, -1, None),                             # causal MHA 2x2048x32
+    (1, 1000, 4, False, -1, None),                             # unmasked GQA, ragged last tile
+    (3, 300, 5, True, -1, None),                               # pairs not a multiple of the group
+    (1, 257, 20, True, 64, None),                              # window, 2.5 groups
+    (1, 16384, 8, True, 1024, (0, 3000, 8000, 9537, 16384)),   # packed sequences with a window
+    (1, 390, 3, False, -1, (0, 33, 161, 390)),                 # packed, unmasked, a 33-row sequence
+])
+def test_tile_schedule_draws_every_key_tile_once(ab, B, S, HKV, causal, window, cu):
+    """The persistent dense kernels draw tiles from a counter and stop at the
+    first invalid draw: every key tile of every (batch, KV head, sequence) must
+    come exactly once before it, with the query-block range the mask needs,
+    and, for dense batches, the longest tiles of each group of pairs first."""
+    seqs = [(0, S)] if cu is None else list(zip(cu[:-1], cu[1:]))
+    want = {(b, g, a, k0) for b in range(B) for g in range(HKV) for (a, e) in seqs for k0 in range(0, e - a, 128)}
+    draws = [ab.tile_schedule(t, B, S, HKV, causal, window, cu) for t in range(_host_tile_bound(B, S, HKV, cu) + 4)]
+    first_invalid = next(i for i, d in enumerate(draws) if not d[0])
+    assert all(not d[0] for d in draws[first_invalid:])
+    got = [d[1:5] for d in draws[:first_invalid]]
+    assert len(got) == len(set(got)) == len(want)
+    assert set(got) == want
+    lens = {a: e - a for (a, e) in seqs}
+    for valid, b, g, a, k0, qlo, nq in draws[:first_invalid]:
+        lo, hi = ab.query_block_range(k0, 128, lens[a], causal, window, 128)
+        assert (qlo, nq) == (lo, hi - lo)
+    if cu is None:  # key block major inside each group of 8 (batch, KV head) pairs
+        pairs = B * HKV
+        for g0 in range(0, pairs, 8):
+            k0s = [d[4] for d in draws[:first_invalid] if g0 <= d[1] * HKV + d[2] < g0 + 8]
+            assert k0s == sorted(k0s)
+
+
+def test_tile_schedule_rejects_bad_sizes(ab):
+    assert ab.tile_schedule(0, 0, 128, 1, True, -1)[0] == 0
+    assert ab.tile_schedule(0, 1, 0, 1, True, -1)[0] == 0
+    assert ab.tile_schedule(-1, 1, 128, 1, True, -1)[0] == 0
+
+
 def test_argument_errors_return_before_any_launch(ab):
     lib = ab.library()
     S = ab._binding.Strides
