@@ -43,7 +43,6 @@ enum DeviceError : int {
   kErrWaitStageFull = 0x103,
   kErrWaitS = 0x104,
   kErrWaitP = 0x105,
-  kErrWaitSRead = 0x106,
   kErrWaitDP = 0x107,
   kErrWaitDS = 0x108,
   kErrWaitDSFree = 0x109,
