@@ -253,10 +253,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// TMEM address: lane in bits 31-16, column in bits 15-0.
-__device__ __forceinline__ uint32_t tmem_at(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
-}
+// TMEM addresses: lane in bits 31-16, column in bits 15-0.
 
 // 32 lanes x 32 bits, 32 consecutive columns per thread (thread i: lane 32 * (warp % 4) + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
