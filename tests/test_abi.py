@@ -160,3 +160,65 @@ def test_argument_errors_return_before_any_launch(ab):
                                    fake, 4096, None) == 3
     # landing: unsupported dtype code
     assert lib.attn_bwd_dq_land(fake, good, 2, 2048, 32, 128, 7, 0.1, fake, 1 << 30, None) == 2
+
+
+def test_sparse_argument_errors_return_before_any_launch(ab):
+    """attn_bwd_sparse and its landing pass reject bad calls with a status and
+    queue nothing (the fake pointers below are never dereferenced)."""
+    lib = ab.library()
+    S = ab._binding.Strides
+    fake = 1 << 20
+    sq = S(4096 * 64 * 576, 64 * 576, 576)
+    skv = S(4096 * 576, 576, 576)
+    sdo = S(4096 * 64 * 512, 64 * 512, 512)
+    sidx = S(4096 * 2048, 2048, 2048)
+
+    def call(q=fake, kv=fake, do=fake, idx=fake, dq=fake, ws=fake, B=1, Sq=4096, SKV=4096, H=64, HKV=1, DQK=576,
+             DV=512, topk=2048, dtype=1, scale=0.04, skv_=skv, ws_bytes=1 << 40):
+        return lib.attn_bwd_sparse(q, sq, kv, skv_, do, sdo, idx, sidx, B, Sq, SKV, H, HKV, DQK, DV, topk, dtype,
+                                   scale, dq, sq, ws, ws_bytes, None)
+
+    assert call(q=None) == 1 and call(idx=None) == 1 and call(ws=None) == 1   # null pointers
+    assert call(H=64, HKV=3) == 1                                              # H not a multiple of HKV
+    assert call(topk=0) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(DQK=512) == 2 and call(DV=448) == 2                            # only the 576 / 512 latent row
+    assert call(H=128, HKV=1) == 2                                             # more than 64 heads per group
+    assert call(dtype=7) == 2
+    assert call(q=fake + 8) == 1                                               # misaligned
+    assert call(skv_=S(4096 * 640, 640, 600)) == 2                             # latent rows not dense
+    assert call(ws_bytes=4096) == 3                                            # workspace too small
+    # landing of dKV: bad sizes, dtype, more than 2^31 rows
+    assert lib.attn_bwd_sparse_land(fake, skv, 1, 4096, 4096, 64, 1, 570, 1, fake, 1 << 40, None) == 1
+    assert lib.attn_bwd_sparse_land(fake, skv, 1, 4096, 4096, 64, 1, 576, 9, fake, 1 << 40, None) == 2
+    assert lib.attn_bwd_sparse_land(fake, skv, 1 << 16, 4096, 1 << 16, 64, 1, 576, 1, fake, 1 << 62, None) == 2
+
+
+def test_landing_and_noalloc_limits_return_before_any_launch(ab):
+    lib = ab.library()
+    S = ab._binding.Strides
+    fake = 1 << 20
+    good = S(2048 * 32 * 128, 32 * 128, 128)
+    # dQ landing: more than 2^31 (b, s, h) rows is refused
+    assert lib.attn_bwd_dq_land(fake, good, 1 << 12, 1 << 12, 1 << 8, 128, 0, 0.1, fake, 1 << 62, None) == 2
+    # no-allocation entry point: sizes past its library-held scratch array, and
+    # an unsupported head dim, are refused before it touches the device
+    m = ab._binding.Mask(1, -1, None, 0)
+    lse = S(32 * 65536, 1, 65536)
+    big = S(65536 * 32 * 128, 32 * 128, 128)
+
+    def noalloc(Sq=65536, D=128):
+        return lib.attn_bwd_gqa_noalloc(fake, big, fake, big, fake, big, fake, big, fake, big, fake, lse, 1, Sq, 32,
+                                        32, D, 0, 0.1, ctypes.byref(m), fake, big, fake, big, fake, big, None)
+
+    assert noalloc() == 3
+    assert noalloc(D=96) == 2
+    # host-buffer entry point: null scratch, unsupported head dim, misaligned scratch
+    def host(scratch=fake, D=128, chunks=4):
+        return lib.attn_bwd_gqa_host(fake, fake, fake, fake, fake, fake, 2, 2048, 32, 32, D, 0, 0.1,
+                                     ctypes.byref(m), fake, fake, fake, scratch, 1 << 40, chunks, None, None, None)
+
+    assert host(scratch=None) == 1
+    assert host(D=96) == 2
+    assert host(scratch=fake + 16) == 1
+    assert lib.attn_bwd_host_scratch_size(2, 2048, 32, 32, 96, 4) == 0
