@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     backward_host,
     check_error,
     dq_land,
+    gqa_main,
     host_scratch_size,
     library,
     preprocess,
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     selftest_timeout,
     sparse_backward,
     sparse_land,
+    sparse_main,
     tile_schedule,
     workspace_size,
 )

@@ -36,14 +36,22 @@ _SIGS = {
     "attn_bwd_workspace_size": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
     "attn_bwd_preprocess": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64,
                                     c_i64, c_i32, c_vp, c_sz, c_vp]),
-    "attn_bwd_gqa": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64,
-                             c_i64, c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, c_sz,
-                             c_vp]),
-    "attn_bwd": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64,
-                         c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd_gqa": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp,
+                             Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, ctypes.POINTER(Mask), c_vp,
+                             Strides, c_vp, Strides, c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides,
+                         c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides,
+                         c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd_gqa_main": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64,
+                                  c_i64, c_i64, c_i32, c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp,
+                                  c_sz, c_vp]),
     "attn_bwd_dq_land": (c_i32, [c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, c_sz, c_vp]),
-    "attn_bwd_sparse": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64,
-                                c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd_sparse": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp,
+                                Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp,
+                                Strides, c_vp, Strides, c_vp, c_sz, c_vp]),
+    "attn_bwd_sparse_main": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64,
+                                     c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32, c_vp, Strides, c_vp, c_sz,
+                                     c_vp]),
     "attn_bwd_sparse_land": (c_i32, [c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_vp, c_sz,
                                      c_vp]),
     "attn_bwd_check_error": (c_i32, [c_vp, c_vp, ctypes.POINTER(c_i32)]),
@@ -56,6 +64,7 @@ _SIGS = {
     "attn_bwd_gqa_noalloc": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides,
                                      c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32,
                                      ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp]),
+    "attn_bwd_noalloc_check_error": (c_i32, [c_vp, ctypes.POINTER(c_i32)]),
     "attn_bwd_host_scratch_size": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64, c_i64]),
     "attn_bwd_gqa_host": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32, c_f32,
                                   ctypes.POINTER(Mask), c_vp, c_vp, c_vp, c_vp, c_sz, c_i64, c_vp, c_vp, c_vp]),
@@ -148,33 +157,23 @@ def preprocess(o, do, lse, workspace, Dq: Optional[int] = None, dkv_elems: int =
             "attn_bwd_preprocess")
 
 
-def attn_bwd_gqa(q, k, v, do, dk, dv, workspace, sm_scale: float, causal: bool = False, window: int = -1,
-                 cu_seqlens=None, stream=None) -> None:
-    """Launch 2: dK, dV written, dQ accumulated in the workspace (see attn_bwd_gqa)."""
+def gqa_main(q, k, v, do, dk, dv, workspace, sm_scale: float, causal: bool = False, window: int = -1,
+             cu_seqlens=None, stream=None) -> None:
+    """Split form, launch 2: dK, dV written, dQ accumulated in the workspace
+    (see attn_bwd_gqa_main)."""
     _dev(q, k, v, do, dk, dv, workspace)
     B, S, HQ, D = q.shape
     HKV = k.shape[2]
     m = _mask(causal, window, cu_seqlens)
-    _status(library().attn_bwd_gqa(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
-                                   do.data_ptr(), _bshd(do), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
-                                   ctypes.byref(m), dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv),
-                                   workspace.data_ptr(), workspace.numel(), _stream(stream)), "attn_bwd_gqa")
-
-
-def attn_bwd(q, k, v, do, dk, dv, workspace, sm_scale: float, causal: bool = False, window: int = -1,
-             cu_seqlens=None, stream=None) -> None:
-    """Launch 2 for multi-head attention (HQ == HKV)."""
-    _dev(q, k, v, do, dk, dv, workspace)
-    B, S, H, D = q.shape
-    m = _mask(causal, window, cu_seqlens)
-    _status(library().attn_bwd(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
-                               do.data_ptr(), _bshd(do), B, S, H, D, _dt(q), float(sm_scale), ctypes.byref(m),
-                               dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv), workspace.data_ptr(),
-                               workspace.numel(), _stream(stream)), "attn_bwd")
+    _status(library().attn_bwd_gqa_main(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
+                                        do.data_ptr(), _bshd(do), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
+                                        ctypes.byref(m), dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv),
+                                        workspace.data_ptr(), workspace.numel(), _stream(stream)),
+            "attn_bwd_gqa_main")
 
 
 def dq_land(dq, workspace, sm_scale: float, stream=None) -> None:
-    """Launch 3: dQ = cast(sm_scale * dQacc)."""
+    """Split form, launch 3: dQ = cast(sm_scale * dQacc)."""
     _dev(dq, workspace)
     B, S, H, D = dq.shape
     _status(library().attn_bwd_dq_land(dq.data_ptr(), _bshd(dq), B, S, H, D, _dt(dq), float(sm_scale),
@@ -182,28 +181,77 @@ def dq_land(dq, workspace, sm_scale: float, stream=None) -> None:
             "attn_bwd_dq_land")
 
 
-def attn_bwd_sparse(q, kv, do, idx, dq, workspace, sm_scale: float, dv_dim: int, stream=None) -> None:
-    """Launch 2 of the top-k sparse path: writes dQ, accumulates dKV (see attn_bwd_sparse)."""
+def attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, workspace, sm_scale: float, causal: bool = False,
+                 window: int = -1, cu_seqlens=None, stream=None) -> None:
+    """The whole dense backward in one call into caller-owned dq, dk, dv (see
+    attn_bwd_gqa): preprocess, main kernel and dQ landing on ``stream``."""
+    _dev(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, S, HQ, D = q.shape
+    HKV = k.shape[2]
+    m = _mask(causal, window, cu_seqlens)
+    _status(library().attn_bwd_gqa(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
+                                   o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(),
+                                   _lse_strides(lse), B, S, HQ, HKV, D, _dt(q), float(sm_scale), ctypes.byref(m),
+                                   dq.data_ptr(), _bshd(dq), dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv),
+                                   workspace.data_ptr(), workspace.numel(), _stream(stream)), "attn_bwd_gqa")
+
+
+def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, sm_scale: float, causal: bool = False, window: int = -1,
+             cu_seqlens=None, stream=None) -> None:
+    """attn_bwd_gqa for multi-head attention (HQ == HKV), through the C entry
+    point attn_bwd."""
+    _dev(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, S, H, D = q.shape
+    m = _mask(causal, window, cu_seqlens)
+    _status(library().attn_bwd(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
+                               o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(), _lse_strides(lse),
+                               B, S, H, D, _dt(q), float(sm_scale), ctypes.byref(m), dq.data_ptr(), _bshd(dq),
+                               dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv), workspace.data_ptr(),
+                               workspace.numel(), _stream(stream)), "attn_bwd")
+
+
+def _idx_strides(idx) -> Strides:
+    if idx.dtype != torch.int32 or idx.dim() != 4 or idx.stride(3) != 1:
+        raise AttnBwdError("idx must be int32 [B, S, HKV, topk] with unit slot stride")
+    return Strides(idx.stride(0), idx.stride(1), idx.stride(2))
+
+
+def sparse_main(q, kv, do, idx, dq, workspace, sm_scale: float, dv_dim: int, stream=None) -> None:
+    """Split form, launch 2 of the top-k sparse path: writes dQ, accumulates
+    dKV (see attn_bwd_sparse_main)."""
     _dev(q, kv, do, idx, dq, workspace)
     B, S, H, DQK = q.shape
     SKV, HKV = kv.shape[1], kv.shape[2]
-    if idx.dtype != torch.int32 or idx.dim() != 4 or idx.stride(3) != 1:
-        raise AttnBwdError("idx must be int32 [B, S, HKV, topk] with unit slot stride")
-    topk = idx.shape[3]
-    _status(library().attn_bwd_sparse(q.data_ptr(), _bshd(q), kv.data_ptr(), _bshd(kv), do.data_ptr(), _bshd(do),
-                                      idx.data_ptr(), Strides(idx.stride(0), idx.stride(1), idx.stride(2)), B, S,
-                                      SKV, H, HKV, DQK, dv_dim, topk, _dt(q), float(sm_scale), dq.data_ptr(),
-                                      _bshd(dq), workspace.data_ptr(), workspace.numel(), _stream(stream)),
-            "attn_bwd_sparse")
+    sidx = _idx_strides(idx)
+    _status(library().attn_bwd_sparse_main(q.data_ptr(), _bshd(q), kv.data_ptr(), _bshd(kv), do.data_ptr(),
+                                           _bshd(do), idx.data_ptr(), sidx, B, S, SKV, H, HKV, DQK, dv_dim,
+                                           idx.shape[3], _dt(q), float(sm_scale), dq.data_ptr(), _bshd(dq),
+                                           workspace.data_ptr(), workspace.numel(), _stream(stream)),
+            "attn_bwd_sparse_main")
 
 
 def sparse_land(dkv, workspace, B: int, S: int, H: int, stream=None) -> None:
-    """Launch 3 of the sparse path: dKV cast from its accumulator."""
+    """Split form, launch 3 of the sparse path: dKV cast from its accumulator."""
     _dev(dkv, workspace)
     _, SKV, HKV, DQK = dkv.shape
     _status(library().attn_bwd_sparse_land(dkv.data_ptr(), _bshd(dkv), B, S, SKV, H, HKV, DQK, _dt(dkv),
                                            workspace.data_ptr(), workspace.numel(), _stream(stream)),
             "attn_bwd_sparse_land")
+
+
+def attn_bwd_sparse(q, kv, o, do, lse, idx, dq, dkv, workspace, sm_scale: float, dv_dim: int,
+                    stream=None) -> None:
+    """The whole top-k sparse backward in one call into caller-owned dq, dkv
+    (see attn_bwd_sparse)."""
+    _dev(q, kv, o, do, lse, idx, dq, dkv, workspace)
+    B, S, H, DQK = q.shape
+    SKV, HKV = kv.shape[1], kv.shape[2]
+    sidx = _idx_strides(idx)
+    _status(library().attn_bwd_sparse(q.data_ptr(), _bshd(q), kv.data_ptr(), _bshd(kv), o.data_ptr(), _bshd(o),
+                                      do.data_ptr(), _bshd(do), lse.data_ptr(), _lse_strides(lse), idx.data_ptr(),
+                                      sidx, B, S, SKV, H, HKV, DQK, dv_dim, idx.shape[3], _dt(q), float(sm_scale),
+                                      dq.data_ptr(), _bshd(dq), dkv.data_ptr(), _bshd(dkv), workspace.data_ptr(),
+                                      workspace.numel(), _stream(stream)), "attn_bwd_sparse")
 
 
 def check_error(workspace, stream=None) -> int:
@@ -245,7 +293,7 @@ def tile_schedule(t: int, B: int, S: int, HKV: int, causal: bool, window: int, c
 
 def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1,
              cu_seqlens=None, workspace=None, stream=None):
-    """dQ, dK, dV of softmax attention: the three launches on one stream.
+    """dQ, dK, dV of softmax attention through the one-call entry point.
 
     q, o, do: [B,S,HQ,D]; k, v: [B,S,HKV,D] (fp16/bf16, CUDA); lse: f32 [B,HQ,S]
     (natural log).  Outputs are new tensors in the input dtype.
@@ -259,16 +307,14 @@ def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    preprocess(o, do, lse, workspace, Dq=D, stream=stream)
-    attn_bwd_gqa(q, k, v, do, dk, dv, workspace, sm_scale, causal, window, cu_seqlens, stream)
-    dq_land(dq, workspace, sm_scale, stream)
+    attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, workspace, sm_scale, causal, window, cu_seqlens, stream)
     return dq, dk, dv
 
 
 def sparse_backward(q, kv, o, do, lse, idx, sm_scale: Optional[float] = None, dv_dim: Optional[int] = None,
                     workspace=None, stream=None):
-    """dQ and dKV of top-k sparse attention over shared latent rows: the
-    preprocess (no dQ accumulator, a dKV one), the sparse kernel, the dKV cast."""
+    """dQ and dKV of top-k sparse attention over shared latent rows through
+    the one-call entry point."""
     _dev(q, kv, o, do, lse, idx)
     B, S, H, DQK = q.shape
     SKV, HKV = kv.shape[1], kv.shape[2]
@@ -280,19 +326,30 @@ def sparse_backward(q, kv, o, do, lse, idx, sm_scale: Optional[float] = None, dv
         workspace = new_workspace(B, S, H, 0, dkv_elems, device=q.device)
     dq = torch.empty_like(q)
     dkv = torch.empty_like(kv)
-    preprocess(o, do, lse, workspace, Dq=0, dkv_elems=dkv_elems, stream=stream)
-    attn_bwd_sparse(q, kv, do, idx, dq, workspace, sm_scale, dv_dim, stream)
-    sparse_land(dkv, workspace, B, S, H, stream)
+    attn_bwd_sparse(q, kv, o, do, lse, idx, dq, dkv, workspace, sm_scale, dv_dim, stream)
     return dq, dkv
 
 
+def noalloc_check_error(stream=None) -> int:
+    """Synchronises the stream; raises if a kernel recorded a device error in
+    the no-allocation entry point's library-held workspace."""
+    code = c_i32(0)
+    st = library().attn_bwd_noalloc_check_error(_stream(stream), ctypes.byref(code))
+    if st != 0:
+        msg = library().attn_bwd_status_string(st).decode()
+        raise AttnBwdError(f"device error: {msg} (site 0x{code.value:x})")
+    return 0
+
+
 def backward_noalloc(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1,
-                     cu_seqlens=None, stream=None):
+                     cu_seqlens=None, stream=None, check: bool = True):
     """dQ, dK, dV through attn_bwd_gqa_noalloc: the library's own device
     workspace instead of a caller-provided one (for callers that cannot
     allocate device memory).  Calls on one device must not overlap on the GPU.
     The output tensors here are allocated by torch for convenience; a caller
-    without an allocator passes its own buffers to the C entry point."""
+    without an allocator passes its own buffers to the C entry point.  With
+    ``check`` the call synchronises and raises on an error the kernels
+    recorded."""
     _dev(q, k, v, o, do, lse)
     B, S, HQ, D = q.shape
     HKV = k.shape[2]
@@ -305,6 +362,8 @@ def backward_noalloc(q, k, v, o, do, lse, sm_scale: Optional[float] = None, caus
                                            _lse_strides(lse), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
                                            ctypes.byref(m), dq.data_ptr(), _bshd(dq), dk.data_ptr(), _bshd(dk),
                                            dv.data_ptr(), _bshd(dv), _stream(stream)), "attn_bwd_gqa_noalloc")
+    if check:
+        noalloc_check_error(stream)
     return dq, dk, dv
 
 

@@ -2,6 +2,11 @@
 // validation, workspace layout, TMA descriptors and launches.  Nothing here
 // allocates device memory or keeps state between calls other than the
 // driver entry point of cuTensorMapEncodeTiled, looked up once.
+//
+// Every launch is prepared by a set-up function that checks its arguments and
+// encodes its tensor maps without touching the device; the one-call forms set
+// up all three launches of a backward before queueing the first, so a bad
+// call queues nothing.
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -116,9 +121,274 @@ bool make_row_map(CUtensorMap* m, const void* base, attn_dtype_t dt, int64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+
 uint64_t wait_limit_ns() { return ab::kWaitTimeoutNs; }
 
+bool dtype_ok(attn_dtype_t dt) { return dt == ATTN_DT_F16 || dt == ATTN_DT_BF16; }
+
+// ---------------------------------------------------------------- set-up of each launch
+
+struct PreSetup {
+  PreprocessParams p;
+  bool bf16;
+};
+
+attn_status_t setup_preprocess(PreSetup* s, const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                               const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t H, int64_t Dv,
+                               int64_t Dq, int64_t dkv_elems, attn_dtype_t dtype, void* workspace,
+                               size_t workspace_bytes) {
+  if (!o || !dO || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || Dv < 8 || Dv % 8 || Dv > 1024 || Dq < 0 || Dq % 8 || dkv_elems < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace) || !strides_ok(so) || !strides_ok(sdo))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || slse.b < 0 || slse.s < 0 || slse.h < 0)
+    return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, S, H, Dq, dkv_elems);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PreprocessParams& p = s->p;
+  p = PreprocessParams{};
+  p.o = static_cast<const uint8_t*>(o);
+  p.so_b = so.b, p.so_s = so.s, p.so_h = so.h;
+  p.dO = static_cast<const uint8_t*>(dO);
+  p.sdo_b = sdo.b, p.sdo_s = sdo.s, p.sdo_h = sdo.h;
+  p.lse = lse;
+  p.sl_b = slse.b, p.sl_s = slse.s, p.sl_h = slse.h;
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.Dv = static_cast<int>(Dv);
+  p.lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<float*>(ws + L.delta_off);
+  p.dq_zero = reinterpret_cast<float4*>(ws + L.dq_off);
+  p.dq_row_n4 = static_cast<int>(Dq / 4);
+  p.zero = reinterpret_cast<float4*>(ws + L.dkv_off);
+  p.zero_n4 = (L.total - L.dkv_off) / 16;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  s->bf16 = dtype == ATTN_DT_BF16;
+  return ATTN_OK;
+}
+
+attn_status_t run_preprocess(const PreSetup& s, void* stream) {
+  return launch_status(launch_preprocess(s.p, s.bf16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+}
+
+struct DenseSetup {
+  DenseParams p;
+  DenseMaps m;
+  bool bf16;
+  int grid;
+};
+
+attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
+                          const void* v, attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S,
+                          int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
+                          const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                          void* workspace, size_t workspace_bytes, bool encode = true) {
+  if (!q || !k || !v || !dO || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || HQ < 1 || HKV < 1 || HQ % HKV != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return ATTN_ERR_UNSUPPORTED;
+  if (HQ / HKV > (dtype == ATTN_DT_BF16 ? ATTN_BWD_MAX_GROUP_BF16 : ATTN_BWD_MAX_GROUP_F16))
+    return ATTN_ERR_UNSUPPORTED;
+  if (S >= (int64_t(1) << 31) || B * HQ * S >= (int64_t(1) << 31) || B > 65535 || HQ > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, k, v, dO, static_cast<const void*>(dk), static_cast<const void*>(dv),
+                          static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  for (const attn_strides_t* st : {&sq, &sk, &sv, &sdo, &sdk, &sdv})
+    if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
+  int causal = 0, window = -1, num_seqs = 0;
+  const int32_t* cu = nullptr;
+  if (mask) {
+    causal = mask->causal ? 1 : 0;
+    window = mask->window_left;
+    cu = mask->cu_seqlens;
+    num_seqs = mask->num_seqs;
+    if (window == 0 || window < -1) return ATTN_ERR_INVALID_ARG;
+    if (cu && (B != 1 || num_seqs < 1 || num_seqs > (1 << 20))) return ATTN_ERR_INVALID_ARG;
+    if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  }
+  const WsLayout L = ws_layout(B, S, HQ, D, 0);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  // key tiles per (batch, KV head): a packed batch may add one partial tile per
+  // sequence.  Persistent CTAs, one per SM, draw tiles from the counter.
+  const int64_t tiles = ((S + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0)) * B * HKV;
+  if (tiles >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (!encode) return ATTN_OK;  // argument checks only: no driver call
+  const int BN = kDenseBN;
+  DenseMaps& m = s->m;
+  if (!make_map(&m.q, q, dtype, B, S, HQ, D, sq, BN) || !make_map(&m.dO, dO, dtype, B, S, HQ, D, sdo, BN) ||
+      !make_map(&m.k, k, dtype, B, S, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, S, HKV, D, sv, kDenseBM))
+    return ATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // dQ partials land as [128 queries x 32 d] boxes staged with a 128-byte swizzle
+  if (!make_acc_map(&m.dq, ws + L.dq_off, B, S, HQ, D, 32, BN)) return ATTN_ERR_INVALID_ARG;
+  DenseParams& p = s->p;
+  p = DenseParams{};
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV);
+  p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D);
+  p.causal = causal, p.window = window, p.cu_seqlens = cu, p.num_seqs = num_seqs;
+  p.sm_scale = sm_scale;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
+  p.dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
+  p.err = &reinterpret_cast<WsHeader*>(ws)->err;
+  p.dk = static_cast<uint8_t*>(dk), p.sdk_b = sdk.b, p.sdk_s = sdk.s, p.sdk_h = sdk.h;
+  p.dv = static_cast<uint8_t*>(dv), p.sdv_b = sdv.b, p.sdv_s = sdv.s, p.sdv_h = sdv.h;
+  p.timeout_ns = wait_limit_ns();
+  p.tile_counter = &reinterpret_cast<WsHeader*>(ws)->tile_counter;
+  p.bn = BN;
+  s->bf16 = dtype == ATTN_DT_BF16;
+  s->grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  return ATTN_OK;
+}
+
+attn_status_t run_dense(const DenseSetup& s, void* stream) {
+  return launch_status(launch_dense(s.p, s.m, s.bf16, s.grid, static_cast<cudaStream_t>(stream)));
+}
+
+struct LandSetup {
+  LandParams p;
+  bool bf16;
+};
+
+attn_status_t setup_dq_land(LandSetup* s, void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
+                            attn_dtype_t dtype, float sm_scale, const void* workspace, size_t workspace_bytes) {
+  if (!dq || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || D < 8 || D % 8) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(dq) || !aligned16(workspace) || !strides_ok(sdq)) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, S, H, D, 0);
+  if (workspace_bytes < static_cast<size_t>(L.dkv_off)) return ATTN_ERR_WORKSPACE;
+  LandParams& p = s->p;
+  p = LandParams{};
+  p.acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + L.dq_off);
+  p.rows = B * S * H;
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.D = static_cast<int>(D);
+  p.out = static_cast<uint8_t*>(dq);
+  p.s_b = sdq.b, p.s_s = sdq.s, p.s_h = sdq.h;
+  p.scale = sm_scale;
+  s->bf16 = dtype == ATTN_DT_BF16;
+  return ATTN_OK;
+}
+
+attn_status_t run_land(const LandSetup& s, void* stream) {
+  return launch_status(launch_land(s.p, s.bf16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+}
+
+struct SparseSetup {
+  SparseParams p;
+  SparseMaps m;
+  bool bf16;
+  int grid;
+};
+
+attn_status_t setup_sparse(SparseSetup* s, const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
+                           const void* dO, attn_strides_t sdo, const int32_t* idx, attn_strides_t sidx, int64_t B,
+                           int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV, int64_t topk,
+                           attn_dtype_t dtype, float sm_scale, void* dq, attn_strides_t sdq, void* workspace,
+                           size_t workspace_bytes) {
+  if (!q || !kv || !dO || !idx || !dq || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || H % HKV != 0 || topk < 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  if (DQK != 576 || DV != 512 || H / HKV > 64) return ATTN_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return ATTN_ERR_UNSUPPORTED;
+  if (B * S * HKV >= (int64_t(1) << 31) || B * SKV * HKV >= (int64_t(1) << 31) || topk >= (int64_t(1) << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, kv, dO, static_cast<const void*>(idx), static_cast<const void*>(dq),
+                          static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  for (const attn_strides_t* st : {&sq, &sdo, &sdq})
+    if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
+  // the latent rows are gathered as rows of a dense [B*SKV*HKV, DQK] matrix
+  if (skv.h < DQK || (skv.h * 2) % 16 || skv.s != HKV * skv.h || skv.b != SKV * skv.s) return ATTN_ERR_UNSUPPORTED;
+  if (sidx.b < 0 || sidx.s < 0 || sidx.h < 0) return ATTN_ERR_INVALID_ARG;
+  const int64_t dkv_elems = B * SKV * HKV * DQK;
+  const WsLayout L = ws_layout(B, S, H, 0, dkv_elems);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  SparseMaps& m = s->m;
+  if (!make_head_map(&m.q, q, dtype, B, S, H, DQK, sq) || !make_head_map(&m.dO, dO, dtype, B, S, H, DV, sdo) ||
+      !make_row_map(&m.kv, kv, dtype, B * SKV * HKV, DQK, skv.h))
+    return ATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SparseParams& p = s->p;
+  p = SparseParams{};
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.SKV = static_cast<int>(SKV);
+  p.H = static_cast<int>(H), p.HKV = static_cast<int>(HKV), p.topk = static_cast<int>(topk);
+  p.gh = static_cast<int>(H / HKV);
+  p.sm_scale = sm_scale;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
+  p.dkv_acc = reinterpret_cast<float*>(ws + L.dkv_off);
+  p.idx = idx;
+  p.si_b = sidx.b, p.si_s = sidx.s, p.si_h = sidx.h;
+  p.dq = static_cast<uint8_t*>(dq);
+  p.sdq_b = sdq.b, p.sdq_s = sdq.s, p.sdq_h = sdq.h;
+  p.err = &reinterpret_cast<WsHeader*>(ws)->err;
+  p.unit_counter = &reinterpret_cast<WsHeader*>(ws)->tile_counter;
+  p.timeout_ns = wait_limit_ns();
+  const int64_t units = B * S * HKV;
+  s->bf16 = dtype == ATTN_DT_BF16;
+  s->grid = static_cast<int>(units < sm_count() ? units : sm_count());
+  return ATTN_OK;
+}
+
+attn_status_t run_sparse(const SparseSetup& s, void* stream) {
+  return launch_status(launch_sparse(s.p, s.m, s.bf16, s.grid, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t setup_sparse_land(LandSetup* s, void* dkv, attn_strides_t sdkv, int64_t B, int64_t S, int64_t SKV,
+                                int64_t H, int64_t HKV, int64_t DQK, attn_dtype_t dtype, const void* workspace,
+                                size_t workspace_bytes) {
+  if (!dkv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || DQK < 8 || DQK % 8) return ATTN_ERR_INVALID_ARG;
+  if (B * SKV * HKV >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(dkv) || !aligned16(workspace) || !strides_ok(sdkv)) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, S, H, 0, B * SKV * HKV * DQK);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
+  LandParams& p = s->p;
+  p = LandParams{};
+  p.acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + L.dkv_off);
+  p.rows = B * SKV * HKV;
+  p.B = static_cast<int>(B), p.S = static_cast<int>(SKV), p.H = static_cast<int>(HKV), p.D = static_cast<int>(DQK);
+  p.out = static_cast<uint8_t*>(dkv);
+  p.s_b = sdkv.b, p.s_s = sdkv.s, p.s_h = sdkv.h;
+  p.scale = 1.f;
+  s->bf16 = dtype == ATTN_DT_BF16;
+  return ATTN_OK;
+}
+
 }  // namespace
+
+namespace ab {
+
+// Every argument check of attn_bwd_gqa, with no device or driver call (the
+// no-allocation entry point runs it before it looks up its scratch array).
+attn_status_t check_gqa_call(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                             attn_strides_t sv, const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                             const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t HQ, int64_t HKV,
+                             int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dq,
+                             attn_strides_t sdq, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                             void* workspace, size_t workspace_bytes) {
+  DenseSetup main;
+  attn_status_t st = setup_dense(&main, q, sq, k, sk, v, sv, dO, sdo, B, S, HQ, HKV, D, dtype, sm_scale, mask, dk,
+                                 sdk, dv, sdv, workspace, workspace_bytes, false);
+  if (st != ATTN_OK) return st;
+  PreSetup pre;
+  st = setup_preprocess(&pre, o, so, dO, sdo, lse, slse, B, S, HQ, D, D, 0, dtype, workspace, workspace_bytes);
+  if (st != ATTN_OK) return st;
+  LandSetup land;
+  return setup_dq_land(&land, dq, sdq, B, S, HQ, D, dtype, sm_scale, workspace, workspace_bytes);
+}
+
+}  // namespace ab
 
 extern "C" {
 
@@ -168,191 +438,104 @@ attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* 
                                   const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t H,
                                   int64_t Dv, int64_t Dq, int64_t dkv_elems, attn_dtype_t dtype, void* workspace,
                                   size_t workspace_bytes, void* stream) {
-  if (!o || !dO || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || H < 1 || Dv < 8 || Dv % 8 || Dv > 1024 || Dq < 0 || Dq % 8 || dkv_elems < 0)
-    return ATTN_ERR_INVALID_ARG;
-  if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace) || !strides_ok(so) || !strides_ok(sdo))
-    return ATTN_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(B, S, H, Dq, dkv_elems);
-  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  PreprocessParams p{};
-  p.o = static_cast<const uint8_t*>(o);
-  p.so_b = so.b, p.so_s = so.s, p.so_h = so.h;
-  p.dO = static_cast<const uint8_t*>(dO);
-  p.sdo_b = sdo.b, p.sdo_s = sdo.s, p.sdo_h = sdo.h;
-  p.lse = lse;
-  p.sl_b = slse.b, p.sl_s = slse.s, p.sl_h = slse.h;
-  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.Dv = static_cast<int>(Dv);
-  p.lse2 = reinterpret_cast<float*>(ws + L.lse2_off);
-  p.delta = reinterpret_cast<float*>(ws + L.delta_off);
-  p.dq_zero = reinterpret_cast<float4*>(ws + L.dq_off);
-  p.dq_row_n4 = static_cast<int>(Dq / 4);
-  p.zero = reinterpret_cast<float4*>(ws + L.dkv_off);
-  p.zero_n4 = (L.total - L.dkv_off) / 16;
-  p.hdr = reinterpret_cast<WsHeader*>(ws);
-  return launch_status(launch_preprocess(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+  PreSetup s;
+  const attn_status_t st =
+      setup_preprocess(&s, o, so, dO, sdo, lse, slse, B, S, H, Dv, Dq, dkv_elems, dtype, workspace, workspace_bytes);
+  return st != ATTN_OK ? st : run_preprocess(s, stream);
 }
 
-attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
-                           attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S,
-                           int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
-                           const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
-                           void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !dO || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || HQ < 1 || HKV < 1 || HQ % HKV != 0) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (S >= (int64_t(1) << 31) || B * HQ * S >= (int64_t(1) << 31) || B > 65535 || HQ > 65535)
-    return ATTN_ERR_UNSUPPORTED;
-  for (const void* ptr : {q, k, v, dO, static_cast<const void*>(dk), static_cast<const void*>(dv),
-                          static_cast<const void*>(workspace)})
-    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
-  for (const attn_strides_t* s : {&sq, &sk, &sv, &sdo, &sdk, &sdv})
-    if (!strides_ok(*s)) return ATTN_ERR_INVALID_ARG;
-  int causal = 0, window = -1, num_seqs = 0;
-  const int32_t* cu = nullptr;
-  if (mask) {
-    causal = mask->causal ? 1 : 0;
-    window = mask->window_left;
-    cu = mask->cu_seqlens;
-    num_seqs = mask->num_seqs;
-    if (window == 0 || window < -1) return ATTN_ERR_INVALID_ARG;
-    if (cu && (B != 1 || num_seqs < 1 || num_seqs > (1 << 20))) return ATTN_ERR_INVALID_ARG;
-  }
-  const WsLayout L = ws_layout(B, S, HQ, D, 0);
-  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
-  const int BN = kDenseBN;
-  DenseMaps m;
-  if (!make_map(&m.q, q, dtype, B, S, HQ, D, sq, BN) || !make_map(&m.dO, dO, dtype, B, S, HQ, D, sdo, BN) ||
-      !make_map(&m.k, k, dtype, B, S, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, S, HKV, D, sv, kDenseBM))
-    return ATTN_ERR_INVALID_ARG;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // dQ partials land as [128 queries x 32 d] boxes staged with a 128-byte swizzle
-  if (!make_acc_map(&m.dq, ws + L.dq_off, B, S, HQ, D, 32, BN)) return ATTN_ERR_INVALID_ARG;
-  DenseParams p{};
-  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV);
-  p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D);
-  p.causal = causal, p.window = window, p.cu_seqlens = cu, p.num_seqs = num_seqs;
-  p.sm_scale = sm_scale;
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
-  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
-  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
-  p.dq_acc = reinterpret_cast<float*>(ws + L.dq_off);
-  p.err = &reinterpret_cast<WsHeader*>(ws)->err;
-  p.dk = static_cast<uint8_t*>(dk), p.sdk_b = sdk.b, p.sdk_s = sdk.s, p.sdk_h = sdk.h;
-  p.dv = static_cast<uint8_t*>(dv), p.sdv_b = sdv.b, p.sdv_s = sdv.s, p.sdv_h = sdv.h;
-  p.timeout_ns = wait_limit_ns();
-  p.tile_counter = &reinterpret_cast<WsHeader*>(ws)->tile_counter;
-  p.bn = BN;
-  // key tiles per (batch, KV head): a packed batch may add one partial tile per
-  // sequence.  Persistent CTAs, one per SM, draw tiles from the counter.
-  const int64_t tiles = ((S + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0)) * B * HKV;
-  if (tiles >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
-  const int64_t grid = tiles < sm_count() ? tiles : sm_count();
-  return launch_status(launch_dense(p, m, dtype == ATTN_DT_BF16, static_cast<int>(grid),
-                                    static_cast<cudaStream_t>(stream)));
-}
-
-attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
-                       attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S, int64_t H,
-                       int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dk,
-                       attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace, size_t workspace_bytes,
-                       void* stream) {
-  return attn_bwd_gqa(q, sq, k, sk, v, sv, dO, sdo, B, S, H, H, D, dtype, sm_scale, mask, dk, sdk, dv, sdv,
-                      workspace, workspace_bytes, stream);
+attn_status_t attn_bwd_gqa_main(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                                attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S,
+                                int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
+                                const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  DenseSetup s;
+  const attn_status_t st = setup_dense(&s, q, sq, k, sk, v, sv, dO, sdo, B, S, HQ, HKV, D, dtype, sm_scale, mask, dk,
+                                       sdk, dv, sdv, workspace, workspace_bytes);
+  return st != ATTN_OK ? st : run_dense(s, stream);
 }
 
 attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
                                attn_dtype_t dtype, float sm_scale, const void* workspace, size_t workspace_bytes,
                                void* stream) {
-  if (!dq || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || H < 1 || D < 8 || D % 8) return ATTN_ERR_INVALID_ARG;
-  if (B * S * H >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(dq) || !aligned16(workspace) || !strides_ok(sdq)) return ATTN_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(B, S, H, D, 0);
-  if (workspace_bytes < static_cast<size_t>(L.dkv_off)) return ATTN_ERR_WORKSPACE;
-  LandParams p{};
-  p.acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + L.dq_off);
-  p.rows = B * S * H;
-  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(H), p.D = static_cast<int>(D);
-  p.out = static_cast<uint8_t*>(dq);
-  p.s_b = sdq.b, p.s_s = sdq.s, p.s_h = sdq.h;
-  p.scale = sm_scale;
-  return launch_status(launch_land(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+  LandSetup s;
+  const attn_status_t st = setup_dq_land(&s, dq, sdq, B, S, H, D, dtype, sm_scale, workspace, workspace_bytes);
+  return st != ATTN_OK ? st : run_land(s, stream);
 }
 
-attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
-                              const void* dO, attn_strides_t sdo, const int32_t* idx, attn_strides_t sidx,
-                              int64_t B, int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV,
-                              int64_t topk, attn_dtype_t dtype, float sm_scale, void* dq, attn_strides_t sdq,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !kv || !dO || !idx || !dq || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || H % HKV != 0 || topk < 1) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
-  if (DQK != 576 || DV != 512 || H / HKV > 64) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (B * S * HKV >= (int64_t(1) << 31) || B * SKV * HKV >= (int64_t(1) << 31) || topk >= (int64_t(1) << 31))
-    return ATTN_ERR_UNSUPPORTED;
-  for (const void* ptr : {q, kv, dO, static_cast<const void*>(idx), static_cast<const void*>(dq),
-                          static_cast<const void*>(workspace)})
-    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
-  for (const attn_strides_t* st : {&sq, &sdo, &sdq})
-    if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
-  // the latent rows are gathered as rows of a dense [B*SKV*HKV, DQK] matrix
-  if (skv.h < DQK || (skv.h * 2) % 16 || skv.s != HKV * skv.h || skv.b != SKV * skv.s) return ATTN_ERR_UNSUPPORTED;
-  if (sidx.b < 0 || sidx.s < 0 || sidx.h < 0) return ATTN_ERR_INVALID_ARG;
-  const int64_t dkv_elems = B * SKV * HKV * DQK;
-  const WsLayout L = ws_layout(B, S, H, 0, dkv_elems);
-  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
-  SparseMaps m;
-  if (!make_head_map(&m.q, q, dtype, B, S, H, DQK, sq) || !make_head_map(&m.dO, dO, dtype, B, S, H, DV, sdo) ||
-      !make_row_map(&m.kv, kv, dtype, B * SKV * HKV, DQK, skv.h))
-    return ATTN_ERR_INVALID_ARG;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  SparseParams p{};
-  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.SKV = static_cast<int>(SKV);
-  p.H = static_cast<int>(H), p.HKV = static_cast<int>(HKV), p.topk = static_cast<int>(topk);
-  p.gh = static_cast<int>(H / HKV);
-  p.sm_scale = sm_scale;
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
-  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
-  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
-  p.dkv_acc = reinterpret_cast<float*>(ws + L.dkv_off);
-  p.idx = idx;
-  p.si_b = sidx.b, p.si_s = sidx.s, p.si_h = sidx.h;
-  p.dq = static_cast<uint8_t*>(dq);
-  p.sdq_b = sdq.b, p.sdq_s = sdq.s, p.sdq_h = sdq.h;
-  p.err = &reinterpret_cast<WsHeader*>(ws)->err;
-  p.unit_counter = &reinterpret_cast<WsHeader*>(ws)->tile_counter;
-  p.timeout_ns = wait_limit_ns();
-  const int64_t units = B * S * HKV;
-  const int grid = static_cast<int>(units < sm_count() ? units : sm_count());
-  return launch_status(launch_sparse(p, m, dtype == ATTN_DT_BF16, grid, static_cast<cudaStream_t>(stream)));
+attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                           attn_strides_t sv, const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                           const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t HQ, int64_t HKV,
+                           int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dq,
+                           attn_strides_t sdq, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  // the three launches are set up (checked, tensor maps encoded) before the first is queued
+  DenseSetup main;
+  attn_status_t st = setup_dense(&main, q, sq, k, sk, v, sv, dO, sdo, B, S, HQ, HKV, D, dtype, sm_scale, mask, dk,
+                                 sdk, dv, sdv, workspace, workspace_bytes);
+  if (st != ATTN_OK) return st;
+  PreSetup pre;
+  st = setup_preprocess(&pre, o, so, dO, sdo, lse, slse, B, S, HQ, D, D, 0, dtype, workspace, workspace_bytes);
+  if (st != ATTN_OK) return st;
+  LandSetup land;
+  st = setup_dq_land(&land, dq, sdq, B, S, HQ, D, dtype, sm_scale, workspace, workspace_bytes);
+  if (st != ATTN_OK) return st;
+  if ((st = run_preprocess(pre, stream)) != ATTN_OK) return st;
+  if ((st = run_dense(main, stream)) != ATTN_OK) return st;
+  return run_land(land, stream);
+}
+
+attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                       attn_strides_t sv, const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                       const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t H, int64_t D,
+                       attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dq, attn_strides_t sdq,
+                       void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return attn_bwd_gqa(q, sq, k, sk, v, sv, o, so, dO, sdo, lse, slse, B, S, H, H, D, dtype, sm_scale, mask, dq, sdq,
+                      dk, sdk, dv, sdv, workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_bwd_sparse_main(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
+                                   const void* dO, attn_strides_t sdo, const int32_t* idx, attn_strides_t sidx,
+                                   int64_t B, int64_t S, int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV,
+                                   int64_t topk, attn_dtype_t dtype, float sm_scale, void* dq, attn_strides_t sdq,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  SparseSetup s;
+  const attn_status_t st = setup_sparse(&s, q, sq, kv, skv, dO, sdo, idx, sidx, B, S, SKV, H, HKV, DQK, DV, topk,
+                                        dtype, sm_scale, dq, sdq, workspace, workspace_bytes);
+  return st != ATTN_OK ? st : run_sparse(s, stream);
 }
 
 attn_status_t attn_bwd_sparse_land(void* dkv, attn_strides_t sdkv, int64_t B, int64_t S, int64_t SKV, int64_t H,
                                    int64_t HKV, int64_t DQK, attn_dtype_t dtype, const void* workspace,
                                    size_t workspace_bytes, void* stream) {
-  if (!dkv || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || SKV < 1 || H < 1 || HKV < 1 || DQK < 8 || DQK % 8) return ATTN_ERR_INVALID_ARG;
-  if (B * SKV * HKV >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(dkv) || !aligned16(workspace) || !strides_ok(sdkv)) return ATTN_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(B, S, H, 0, B * SKV * HKV * DQK);
-  if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
-  LandParams p{};
-  p.acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + L.dkv_off);
-  p.rows = B * SKV * HKV;
-  p.B = static_cast<int>(B), p.S = static_cast<int>(SKV), p.H = static_cast<int>(HKV), p.D = static_cast<int>(DQK);
-  p.out = static_cast<uint8_t*>(dkv);
-  p.s_b = sdkv.b, p.s_s = sdkv.s, p.s_h = sdkv.h;
-  p.scale = 1.f;
-  return launch_status(launch_land(p, dtype == ATTN_DT_BF16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
+  LandSetup s;
+  const attn_status_t st =
+      setup_sparse_land(&s, dkv, sdkv, B, S, SKV, H, HKV, DQK, dtype, workspace, workspace_bytes);
+  return st != ATTN_OK ? st : run_land(s, stream);
+}
+
+attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv, const void* o,
+                              attn_strides_t so, const void* dO, attn_strides_t sdo, const float* lse,
+                              attn_strides_t slse, const int32_t* idx, attn_strides_t sidx, int64_t B, int64_t S,
+                              int64_t SKV, int64_t H, int64_t HKV, int64_t DQK, int64_t DV, int64_t topk,
+                              attn_dtype_t dtype, float sm_scale, void* dq, attn_strides_t sdq, void* dkv,
+                              attn_strides_t sdkv, void* workspace, size_t workspace_bytes, void* stream) {
+  SparseSetup main;
+  attn_status_t st = setup_sparse(&main, q, sq, kv, skv, dO, sdo, idx, sidx, B, S, SKV, H, HKV, DQK, DV, topk, dtype,
+                                  sm_scale, dq, sdq, workspace, workspace_bytes);
+  if (st != ATTN_OK) return st;
+  const int64_t dkv_elems = B * SKV * HKV * DQK;
+  PreSetup pre;
+  st = setup_preprocess(&pre, o, so, dO, sdo, lse, slse, B, S, H, DV, 0, dkv_elems, dtype, workspace,
+                        workspace_bytes);
+  if (st != ATTN_OK) return st;
+  LandSetup land;
+  st = setup_sparse_land(&land, dkv, sdkv, B, S, SKV, H, HKV, DQK, dtype, workspace, workspace_bytes);
+  if (st != ATTN_OK) return st;
+  if ((st = run_preprocess(pre, stream)) != ATTN_OK) return st;
+  if ((st = run_sparse(main, stream)) != ATTN_OK) return st;
+  return run_land(land, stream);
 }
 
 attn_status_t attn_bwd_check_error(const void* workspace, void* stream, int32_t* device_code) {

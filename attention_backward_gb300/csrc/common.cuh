@@ -54,6 +54,7 @@ enum DeviceError : int {
   kErrWaitKVFree = 0x10F,
   kErrWaitStage = 0x110,
   kErrWaitDKVFree = 0x111,
+  kErrWaitTail = 0x112,
   kErrAlign = 0x1FE,
   kErrSelftest = 0x1FF,
   kErrSparseBase = 0x200,
@@ -84,5 +85,15 @@ __host__ __device__ inline void query_block_range(int k0, int bk, int len, int c
 
 // Sequence bounds of batch row b / packed sequence n, clamped to [0, S].
 __host__ __device__ inline int clamp_pos(int x, int S) { return x < 0 ? 0 : (x > S ? S : x); }
+
+// Rows [r0, r1) of a block of ``rows`` positions starting at position ``base``
+// of a packed batch that lie in [tail0, S): past the last sequence but inside
+// the tensor, so a TMA load reads whatever the caller left there (rows past S
+// read zeros).  Empty (r0 >= r1) when the block does not reach the tail.
+__host__ __device__ inline void tail_rows(int base, int rows, int tail0, int S, int* r0, int* r1) {
+  const int a = tail0 - base, e = S - base;
+  *r0 = a < 0 ? 0 : a;
+  *r1 = e < rows ? e : rows;
+}
 
 }  // namespace ab

@@ -116,6 +116,7 @@ enum Bar : int {
   DKV_FULL = STG_FULLB0 + ST,
   DKV_FREE,
   DRAIN,
+  TAIL,             // the producer's own: loads of tiles that overhang the last packed sequence
   NUM_BARS
 };
 static_assert(NUM_BARS <= NBAR, "barrier storage");
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     mbar_init(&bars[DKV_FULL], 1);
     mbar_init(&bars[DKV_FREE], 4);  // the 4 dQ epilogue warps land dK/dV
     mbar_init(&bars[DRAIN], 1);
+    mbar_init(&bars[TAIL], 1);
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -182,6 +184,35 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
 #pragma unroll
     for (int i = 0; i < ST; ++i) pend_full[i] = pend_d[i] = -1;
     int kv_pend = -1;
+    // Rows from tail0 to S belong to no packed sequence and may hold anything:
+    // a tile or query block that reaches them is loaded onto the producer's
+    // own barrier, those rows are zeroed, and only then is it published, so no
+    // MMA multiplies them (a zero P or dS times a NaN is NaN).
+    const int tail0 = p.cu_seqlens ? clamp_pos(p.cu_seqlens[p.num_seqs], p.S) : p.S;
+    uint32_t tail_ph = 0;
+    int tail_pend = -1;
+    // loads the tile onto TAIL, waits, zeroes rows [r0, r1) of its slabs and
+    // publishes it with a plain arrival on ``full``
+    auto load_zeroed = [&](uint8_t* dst0, const CUtensorMap* m0, uint8_t* dst1, const CUtensorMap* m1, int h_,
+                           int pos, int b_, int r0, int r1, uint64_t* full) -> bool {
+      const uint32_t bytes = (dst1 ? 2 : 1) * Q_TILE;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[TAIL], bytes);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          tma_load_4d(dst0 + s * SLAB, m0, &bars[TAIL], s * 64, h_, pos, b_);
+          if (dst1) tma_load_4d(dst1 + s * SLAB, m1, &bars[TAIL], s * 64, h_, pos, b_);
+        }
+      }
+      tail_pend = tail_ph & 1;
+      if (!mbar_wait_warp(&bars[TAIL], tail_ph & 1, wc, kErrWaitTail)) return false;
+      tail_pend = -1;
+      ++tail_ph;
+      zero_tile_rows(dst0, 2, SLAB, r0, r1, lane);
+      if (dst1) zero_tile_rows(dst1, 2, SLAB, r0, r1, lane);
+      if (lane == 0) mbar_arrive(full);
+      return true;
+    };
     uint32_t gs = 0;
     bool ok = true;
     for (int tc = 0; ok; ++tc) {
@@ -197,7 +228,14 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       }
       if (!ti.valid) break;
       if (tc >= 1 && !(ok = mbar_wait_warp(&bars[KV_FREE], (tc - 1) & 1, wc, kErrWaitKVFree))) break;
-      if (lane == 0) {
+      int kr0, kr1;
+      tail_rows(ti.seq_start + ti.k0, BM, tail0, p.S, &kr0, &kr1);
+      if (kr0 < kr1) {
+        static_assert(KV_TILE == Q_TILE, "one tail load size");
+        if (!(ok = load_zeroed(sm + OFF_K, &maps.k, sm + OFF_V, &maps.v, ti.g, ti.seq_start + ti.k0, ti.b, kr0, kr1,
+                               &bars[KV_FULL])))
+          break;
+      } else if (lane == 0) {
         mbar_arrive_expect_tx(&bars[KV_FULL], 2 * KV_TILE);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -229,7 +267,13 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           break;
         const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
         uint8_t* sq = sm + OFF_STAGE + st * STAGE;
-        if (lane == 0) {
+        int qr0, qr1;
+        tail_rows(ti.seq_start + q0, BN, tail0, p.S, &qr0, &qr1);
+        if (qr0 < qr1) {
+          if (!(ok = load_zeroed(sq, &maps.q, nullptr, nullptr, h, ti.seq_start + q0, ti.b, qr0, qr1,
+                                 &bars[FULL0 + st])))
+            break;
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(&bars[FULL0 + st], Q_TILE);
 #pragma unroll
           for (int s = 0; s < 2; ++s)
@@ -264,7 +308,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (gs >= static_cast<uint32_t>(ST) &&
             !(ok = mbar_wait_warp(&bars[EMPTYD0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
           break;
-        if (lane == 0) {
+        if (qr0 < qr1) {
+          if (!(ok = load_zeroed(sq + Q_TILE, &maps.dO, nullptr, nullptr, h, ti.seq_start + q0, ti.b, qr0, qr1,
+                                 &bars[FULLD0 + st])))
+            break;
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(&bars[FULLD0 + st], Q_TILE);
 #pragma unroll
           for (int s = 0; s < 2; ++s)
@@ -276,6 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     }
     // loads still in flight land before the CTA exits
     if (lane == 0) {
+      if (tail_pend >= 0) mbar_drain(&bars[TAIL], tail_pend);
       if (kv_pend >= 0) mbar_drain(&bars[KV_FULL], kv_pend);
 #pragma unroll
       for (int i = 0; i < ST; ++i) {

@@ -117,6 +117,7 @@ enum Bar : int {
   DRAIN,
   DP_FREE,
   DK_DONE,
+  TAIL,             // the producer's own: loads of tiles that overhang the last packed sequence
   NUM_BARS
 };
 static_assert(NUM_BARS <= 32, "barrier storage");
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[DRAIN], 1);
     mbar_init(&bars[DP_FREE], 8);
     mbar_init(&bars[DK_DONE], 1);
+    mbar_init(&bars[TAIL], 1);
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -184,6 +186,32 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
 #pragma unroll
     for (int i = 0; i < ST; ++i) pend_full[i] = -1;
     int kv_pend = -1;
+    // Rows from tail0 to S belong to no packed sequence and may hold anything:
+    // a tile or query block that reaches them is loaded onto the producer's
+    // own barrier, those rows are zeroed, and only then is it published, so no
+    // MMA multiplies them (a zero P or dS times a NaN is NaN).
+    const int tail0 = p.cu_seqlens ? clamp_pos(p.cu_seqlens[p.num_seqs], p.S) : p.S;
+    uint32_t tail_ph = 0;
+    int tail_pend = -1;
+    // loads two one-slab tiles onto TAIL, waits, zeroes rows [r0, r1) of both
+    // and publishes them with a plain arrival on ``full``
+    auto load_zeroed = [&](uint8_t* dst0, const CUtensorMap* m0, uint8_t* dst1, const CUtensorMap* m1, int h_,
+                           int pos, int b_, int r0, int r1, uint64_t* full) -> bool {
+      static_assert(C::NSLAB == 1 && C::KV_TILE == C::Q_TILE, "one-slab tiles of one size");
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[TAIL], 2 * C::Q_TILE);
+        tma_load_4d(dst0, m0, &bars[TAIL], 0, h_, pos, b_);
+        tma_load_4d(dst1, m1, &bars[TAIL], 0, h_, pos, b_);
+      }
+      tail_pend = tail_ph & 1;
+      if (!mbar_wait_warp(&bars[TAIL], tail_ph & 1, wc, kErrWaitTail)) return false;
+      tail_pend = -1;
+      ++tail_ph;
+      zero_tile_rows(dst0, 1, C::Q_SLAB, r0, r1, lane);
+      zero_tile_rows(dst1, 1, C::Q_SLAB, r0, r1, lane);
+      if (lane == 0) mbar_arrive(full);
+      return true;
+    };
     uint32_t gs = 0;
     bool ok = true;
     for (int tc = 0; ok; ++tc) {
@@ -199,7 +227,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       }
       if (!ti.valid) break;
       if (tc >= 1 && !(ok = mbar_wait_warp(&bars[KV_FREE], (tc - 1) & 1, wc, kErrWaitKVFree))) break;
-      if (lane == 0) {
+      int kr0, kr1;
+      tail_rows(ti.seq_start + ti.k0, BM, tail0, p.S, &kr0, &kr1);
+      if (kr0 < kr1) {
+        if (!(ok = load_zeroed(sm + C::OFF_K, &maps.k, sm + C::OFF_V, &maps.v, ti.g, ti.seq_start + ti.k0, ti.b, kr0,
+                               kr1, &bars[KV_FULL])))
+          break;
+      } else if (lane == 0) {
         mbar_arrive_expect_tx(&bars[KV_FULL], 2 * C::KV_TILE);
 #pragma unroll
         for (int s = 0; s < C::NSLAB; ++s) {
@@ -233,7 +267,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             !(ok = mbar_wait_warp(&bars[EMPTY0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
           break;
         const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
-        if (lane == 0) {
+        int qr0, qr1;
+        tail_rows(ti.seq_start + q0, BN, tail0, p.S, &qr0, &qr1);
+        if (qr0 < qr1) {
+          if (!(ok = load_zeroed(sm + C::OFF_Q + st * C::Q_TILE, &maps.q, sm + C::OFF_DO + st * C::Q_TILE, &maps.dO, h,
+                                 ti.seq_start + q0, ti.b, qr0, qr1, &bars[FULL0 + st])))
+            break;
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(&bars[FULL0 + st], 2 * C::Q_TILE);
 #pragma unroll
           for (int s = 0; s < C::NSLAB; ++s) {
@@ -272,6 +312,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     }
     // loads still in flight land before the CTA exits
     if (lane == 0) {
+      if (tail_pend >= 0) mbar_drain(&bars[TAIL], tail_pend);
       if (kv_pend >= 0) mbar_drain(&bars[KV_FULL], kv_pend);
 #pragma unroll
       for (int i = 0; i < ST; ++i)

@@ -6,7 +6,7 @@
 // head, dQ and delta per query head).  Chunk i goes through three streams:
 //
 //   copy-in   strided head slices of q, k, v, o, dO, LSE -> contiguous chunk buffers
-//   compute   preprocess, main kernel, dQ landing on the chunk
+//   compute   attn_bwd_gqa (preprocess, main kernel, dQ landing) on the chunk
 //   copy-out  contiguous dQ, dK, dV of the chunk -> strided host slices
 //
 // with two buffer slots, so that the copy-in of chunk i+1 and the copy-out of
@@ -14,6 +14,7 @@
 // with pageable memory the copies are correct but do not overlap.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <vector>
 
@@ -75,7 +76,10 @@ extern "C" attn_status_t attn_bwd_gqa_host(const void* q, const void* k, const v
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !scratch) return ATTN_ERR_INVALID_ARG;
   if (!shape_ok(B, S, HQ, HKV, D, chunks)) return D == 64 || D == 128 ? ATTN_ERR_INVALID_ARG : ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (mask && (mask->window_left == 0 || mask->window_left < -1 || (mask->cu_seqlens && B != 1)))
+  if (HQ / HKV > (dtype == ATTN_DT_BF16 ? ATTN_BWD_MAX_GROUP_BF16 : ATTN_BWD_MAX_GROUP_F16)) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  if (mask && (mask->window_left == 0 || mask->window_left < -1 ||
+               (mask->cu_seqlens && (B != 1 || mask->num_seqs < 1 || mask->num_seqs > (1 << 20)))))
     return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
   const HostLayout L = host_layout(B, S, HQ, HKV, D, chunks);
@@ -126,12 +130,9 @@ extern "C" attn_status_t attn_bwd_gqa_host(const void* q, const void* k, const v
     // ---- compute on the contiguous chunk
     if (!ok(cudaStreamWaitEvent(sc, copied_in(i), 0))) break;
     const attn_strides_t sqo{S * hqn * D, hqn * D, D}, skv{S * hkn * D, hkn * D, D}, sl{hqn * S, 1, S};
-    st = attn_bwd_preprocess(slot + L.o, sqo, slot + L.dO, sqo, reinterpret_cast<const float*>(slot + L.lse), sl, B,
-                             S, hqn, D, D, 0, dtype, ws, L.ws_bytes, sc);
-    if (st == ATTN_OK)
-      st = attn_bwd_gqa(slot + L.q, sqo, slot + L.k, skv, slot + L.v, skv, slot + L.dO, sqo, B, S, hqn, hkn, D, dtype,
-                        sm_scale, mask, slot + L.dk, skv, slot + L.dv, skv, ws, L.ws_bytes, sc);
-    if (st == ATTN_OK) st = attn_bwd_dq_land(slot + L.dq, sqo, B, S, hqn, D, dtype, sm_scale, ws, L.ws_bytes, sc);
+    st = attn_bwd_gqa(slot + L.q, sqo, slot + L.k, skv, slot + L.v, skv, slot + L.o, sqo, slot + L.dO, sqo,
+                      reinterpret_cast<const float*>(slot + L.lse), sl, B, S, hqn, hkn, D, dtype, sm_scale, mask,
+                      slot + L.dq, sqo, slot + L.dk, skv, slot + L.dv, skv, ws, L.ws_bytes, sc);
     if (st != ATTN_OK || !ok(cudaEventRecord(computed(i), sc))) break;
     // ---- copy-out
     if (!ok(cudaStreamWaitEvent(so, computed(i), 0))) break;

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include "attn_bwd.h"
 #include "common.cuh"
 
 namespace ab {
@@ -92,6 +93,14 @@ cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, in
 // p.D == 128 here and runs head dim 64 itself (dense_bwd.cu).
 cudaError_t launch_dense128(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st);
 cudaError_t launch_selftest_timeout(int* err, uint64_t timeout_ns, cudaStream_t st);
+
+// Every argument check of attn_bwd_gqa (api.cu), with no device or driver call.
+attn_status_t check_gqa_call(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                             attn_strides_t sv, const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                             const float* lse, attn_strides_t slse, int64_t B, int64_t S, int64_t HQ, int64_t HKV,
+                             int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dq,
+                             attn_strides_t sdq, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
+                             void* workspace, size_t workspace_bytes);
 
 // Block sizes of both dense kernels: keys per tile, and queries per step
 // (every MMA at N = 128; 64-query steps with a double-buffered S^T measured

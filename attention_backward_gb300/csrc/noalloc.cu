@@ -13,13 +13,17 @@
 //
 // The array's name in host code is only a host-side stand-in for the device
 // symbol, so the device address is looked up with cudaGetSymbolAddress, once
-// per device, with that device current, on the first call made on it.
+// per device, with that device current, on the first call made on it, and
+// kept for the life of the process (a device reset would make it stale).
+// Errors that the kernels record (a bounded wait that ran out) land in the
+// array's workspace header; attn_bwd_noalloc_check_error reads them back.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "attn_bwd.h"
+#include "kernels.h"
 
 namespace {
 
@@ -47,8 +51,6 @@ attn_status_t scratch_on_current_device(void** out) {
   return ATTN_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
@@ -58,27 +60,31 @@ extern "C" attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq, 
                                               int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask,
                                               void* dq, attn_strides_t sdq, void* dk, attn_strides_t sdk, void* dv,
                                               attn_strides_t sdv, void* stream) {
-  // Checks that the three launches below would otherwise reject one by one,
-  // made first so that a bad call queues nothing.
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  // Every argument, the size limit included, is checked before the device is
+  // touched; the aligned placeholder stands in for the array's address, which
+  // the checks never dereference.
   if (B < 1 || S < 1 || HQ < 1 || HKV < 1 || HQ % HKV != 0) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
-  for (const void* p : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
-                        static_cast<const void*>(dv)})
-    if (!aligned16(p)) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_bwd_workspace_size(B, S, HQ, D, 0);
   if (need == 0 || need > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
-
+  attn_status_t st = ab::check_gqa_call(q, sq, k, sk, v, sv, o, so, dO, sdo, lse, slse, B, S, HQ, HKV, D, dtype,
+                                        sm_scale, mask, dq, sdq, dk, sdk, dv, sdv, reinterpret_cast<void*>(256),
+                                        kNoAllocScratchBytes);
+  if (st != ATTN_OK) return st;
   void* ws = nullptr;
-  attn_status_t st = scratch_on_current_device(&ws);
+  st = scratch_on_current_device(&ws);
   if (st != ATTN_OK) return st;
   // The preprocess clears the error word, the tile counter and the dQ
   // accumulator, so the contents a previous call left behind do not matter.
-  st = attn_bwd_preprocess(o, so, dO, sdo, lse, slse, B, S, HQ, D, D, 0, dtype, ws, kNoAllocScratchBytes, stream);
+  return attn_bwd_gqa(q, sq, k, sk, v, sv, o, so, dO, sdo, lse, slse, B, S, HQ, HKV, D, dtype, sm_scale, mask, dq,
+                      sdq, dk, sdk, dv, sdv, ws, kNoAllocScratchBytes, stream);
+}
+
+extern "C" attn_status_t attn_bwd_noalloc_check_error(void* stream, int32_t* device_code) {
+  if (device_code) *device_code = 0;
+  void* ws = nullptr;
+  const attn_status_t st = scratch_on_current_device(&ws);
   if (st != ATTN_OK) return st;
-  st = attn_bwd_gqa(q, sq, k, sk, v, sv, dO, sdo, B, S, HQ, HKV, D, dtype, sm_scale, mask, dk, sdk, dv, sdv, ws,
-                    kNoAllocScratchBytes, stream);
-  if (st != ATTN_OK) return st;
-  return attn_bwd_dq_land(dq, sdq, B, S, HQ, D, dtype, sm_scale, ws, kNoAllocScratchBytes, stream);
+  // the array starts with a workspace header, whose error word the kernels set
+  return attn_bwd_check_error(ws, stream, device_code);
 }

@@ -278,6 +278,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Zeroes rows [r0, r1) of ``nslab`` 128-byte-swizzled slabs of ``slab_bytes``
+// each (whole warp; a row is 128 contiguous bytes of a slab, whatever the
+// swizzle), then orders the stores before later async-proxy reads of the tile.
+__device__ __forceinline__ void zero_tile_rows(uint8_t* tile, int nslab, int slab_bytes, int r0, int r1, int lane) {
+  const int n = (r1 - r0) * 8;
+  for (int s = 0; s < nslab; ++s)
+    for (int i = lane; i < n; i += 32)
+      *reinterpret_cast<uint4*>(tile + s * slab_bytes + (r0 + i / 8) * 128 + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // Byte offset of the 16-byte chunk ``chunk`` (0..7) of row ``row`` inside a
 // 128-byte-swizzled tile whose base is 1024-byte aligned.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {

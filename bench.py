@@ -141,9 +141,42 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def source_hash(kernel_src: str) -> str:
+    """sha256 prefix over a kernel's .cu file and every header it includes,
+    transitively (quoted includes found in the library's csrc/ and include/),
+    in first-include order: a DRAM record stays valid only while none of them
+    changed."""
+    dirs = [os.path.dirname(kernel_src), os.path.join(ROOT, "include")]
+    seen, order = set(), []
+
+    def visit(path):
+        if path in seen:
+            return
+        seen.add(path)
+        order.append(path)
+        with open(path) as f:
+            for line in f:
+                s = line.strip()
+                if s.startswith("#include \""):
+                    name = s.split('"')[1]
+                    for d in dirs:
+                        cand = os.path.join(d, name)
+                        if os.path.exists(cand):
+                            visit(cand)
+                            break
+
+    visit(kernel_src)
+    h = hashlib.sha256()
+    for path in order:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel_src: str, name: str):
     """DRAM bytes per launch of ``name`` from the committed ncu summary, only if
-    it was taken on the current kernel source (matching hash)."""
+    it was taken on the current kernel sources (matching hash over the .cu file
+    and its headers)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -151,9 +184,7 @@ def traffic_record(kernel_src: str, name: str):
         rec = json.load(f).get(name)
     if not rec:
         return None
-    with open(kernel_src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec.get("dram_bytes_per_launch") if rec.get("source_sha256_16") == h else None
+    return rec.get("dram_bytes_per_launch") if rec.get("source_sha256_16") == source_hash(kernel_src) else None
 
 
 # ------------------------------------------------------------------ inputs (GPU arm)
@@ -275,7 +306,7 @@ def time_dense(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
         ev[0].record(stream)
         ab.preprocess(to, tdo, lse, ws, Dq=w.D, stream=stream)
         ev[1].record(stream)
-        ab.attn_bwd_gqa(tq, tk, tv, tdo, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
+        ab.gqa_main(tq, tk, tv, tdo, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
         ev[2].record(stream)
         ab.dq_land(dq, ws, w.sm_scale, stream)
         ev[3].record(stream)
@@ -299,7 +330,7 @@ def time_sparse(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
         ev[0].record(stream)
         ab.preprocess(to, tdo, lse, ws, Dq=0, dkv_elems=dkv_elems, stream=stream)
         ev[1].record(stream)
-        ab.attn_bwd_sparse(tq, tkv, tdo, tidx, dq, ws, w.sm_scale, w.Dv, stream)
+        ab.sparse_main(tq, tkv, tdo, tidx, dq, ws, w.sm_scale, w.Dv, stream)
         ev[2].record(stream)
         ab.sparse_land(dkv, ws, w.B, w.S, w.HQ, stream)
         ev[3].record(stream)
@@ -308,11 +339,17 @@ def time_sparse(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
     return _stage_times(per) | {"tensors": (tq, tkv, to, tdo, lse, tidx), "idx": idx}
 
 
+def _pct(xs):
+    """Median and the 10th / 90th percentiles of a list of times (ms)."""
+    return {"p10": float(np.percentile(xs, 10)), "median": float(np.median(xs)), "p90": float(np.percentile(xs, 90))}
+
+
 def _stage_times(per):
     tot = [e[0].elapsed_time(e[3]) for e in per]
-    return {"ms_step": float(np.mean(tot)), "ms_step_median": float(np.median(tot)),
+    main = [e[1].elapsed_time(e[2]) for e in per]
+    return {"ms_step": float(np.mean(tot)), "ms_step_pct": _pct(tot),
             "ms_pre": float(np.mean([e[0].elapsed_time(e[1]) for e in per])),
-            "ms_main": float(np.mean([e[1].elapsed_time(e[2]) for e in per])),
+            "ms_main": float(np.mean(main)), "ms_main_pct": _pct(main),
             "ms_land": float(np.mean([e[2].elapsed_time(e[3]) for e in per]))}
 
 
@@ -366,31 +403,94 @@ def time_e2e(w, tensors, steps, device, chunks=4):
 
 
 def cpu_oracle_sample(w, budget_s=12.0):
-    """The oracle backward timed on the host cores over a bounded sample of the
-    workload (a prefix of the query heads, all batch rows); inputs from the
-    seeded generator and the oracle's own forward (not timed)."""
+    """The oracle timed on the host cores over a bounded sample of workload
+    ``w``; inputs from the seeded generator and the oracle's own forward (not
+    timed).  Returns (TFLOP/s of the workload's counted FLOPs, seconds timed,
+    description of the sample).
+
+    Short dense rows (S <= 4096, one sequence per batch row): whole query heads
+    (a prefix, whole KV groups).  Long or packed rows: one KV group's query
+    heads on seeded rows, dQ rows and dK/dV rows evaluated separately by the
+    oracle (7 matrix products per row instead of the 5 of a whole-head
+    evaluation), extrapolated linearly by rows and heads.  Sparse: the whole
+    backward of a seeded sample of tokens, extrapolated by valid (token, slot)
+    pairs."""
     import oracle
     from attention_backward_gb300 import inputs
 
+    if w.kind == "sparse":
+        return _cpu_sparse_sample(w, budget_s)
     q, k, v, do = inputs.dense_inputs(w)
     mask = dict(causal=w.causal, window=w.window, cu_seqlens=w.cu_seqlens)
-    # calibrate on one head, then time as many heads as fit the budget
-    o1, l1 = oracle.forward(q[:, :, :1], k[:, :, :1], v[:, :, :1], w.sm_scale, **mask)
-    o1 = inputs.round_to_dtype(o1, w.dtype)
-    t0 = time.perf_counter()
-    oracle.backward(q[:, :, :1], k[:, :, :1], v[:, :, :1], o1, do[:, :, :1], l1, w.sm_scale, **mask)
-    t1 = time.perf_counter() - t0
-    nh = int(max(1, min(w.HQ, budget_s // max(t1, 1e-3))))
     G = w.HQ // w.HKV
-    nh = max(G, (nh // G) * G)
-    qs, ks, vs, dos = q[:, :, :nh], k[:, :, :nh // G], v[:, :, :nh // G], do[:, :, :nh]
+    if w.S <= 4096 and w.cu_seqlens is None:
+        # calibrate on one head, then time as many whole KV groups as fit the budget
+        o1, l1 = oracle.forward(q[:, :, :1], k[:, :, :1], v[:, :, :1], w.sm_scale, **mask)
+        o1 = inputs.round_to_dtype(o1, w.dtype)
+        t0 = time.perf_counter()
+        oracle.backward(q[:, :, :1], k[:, :, :1], v[:, :, :1], o1, do[:, :, :1], l1, w.sm_scale, **mask)
+        t1 = time.perf_counter() - t0
+        nh = int(max(1, min(w.HQ, budget_s // max(t1, 1e-3))))
+        nh = max(G, (nh // G) * G)
+        qs, ks, vs, dos = q[:, :, :nh], k[:, :, :nh // G], v[:, :, :nh // G], do[:, :, :nh]
+        o, lse = oracle.forward(qs, ks, vs, w.sm_scale, **mask)
+        o = inputs.round_to_dtype(o, w.dtype)
+        t0 = time.perf_counter()
+        oracle.backward(qs, ks, vs, o, dos, lse, w.sm_scale, **mask)
+        el = time.perf_counter() - t0
+        frac = nh / w.HQ
+        return (dense_flops(w) * frac / el / 1e12, el,
+                f"{nh} of {w.HQ} query heads x {w.B} batch rows of {w.name}, whole heads, {el:.1f} s of float64 numpy")
+    # long rows: the first KV group's heads on seeded rows
+    qs, ks, vs, dos = q[:, :, :G], k[:, :, :1], v[:, :, :1], do[:, :, :G]
     o, lse = oracle.forward(qs, ks, vs, w.sm_scale, **mask)
     o = inputs.round_to_dtype(o, w.dtype)
+    rng = np.random.default_rng(w.seed)
+    if w.cu_seqlens is not None:  # rows inside sequences only
+        inside = np.concatenate([np.arange(a, e) for a, e in zip(w.cu_seqlens[:-1], w.cu_seqlens[1:])])
+    else:
+        inside = np.arange(w.S)
+    rows = np.sort(rng.choice(inside, size=min(64, inside.size), replace=False))
     t0 = time.perf_counter()
-    oracle.backward(qs, ks, vs, o, dos, lse, w.sm_scale, **mask)
+    oracle.backward(qs, ks, vs, o, dos, lse, w.sm_scale, q_rows=rows, k_rows=rows, **mask)
+    t1 = time.perf_counter() - t0
+    n = int(min(inside.size, max(64, rows.size * budget_s / max(t1, 1e-3))))
+    rows = np.sort(rng.choice(inside, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle.backward(qs, ks, vs, o, dos, lse, w.sm_scale, q_rows=rows, k_rows=rows, **mask)
     el = time.perf_counter() - t0
-    frac = nh / w.HQ
-    return dense_flops(w) * frac / el / 1e12, el, nh
+    frac = (G / w.HQ) * (rows.size / inside.size) / w.B
+    return (dense_flops(w) * frac / el / 1e12, el,
+            f"{rows.size} seeded rows (dQ rows and dK/dV rows) of query heads 0-{G - 1} (one KV group) of "
+            f"{w.name}, {el:.1f} s of float64 numpy, extrapolated linearly to every row and head")
+
+
+def _cpu_sparse_sample(w, budget_s):
+    """The oracle's whole sparse backward (dQ and the dKV contributions) over
+    the tokens of a seeded sample, extrapolated by valid (token, slot) pairs."""
+    import oracle
+    from attention_backward_gb300 import inputs
+
+    q, kv, do, idx = inputs.sparse_inputs(w)
+    rng = np.random.default_rng(w.seed)
+    valid = lambda ix: int(((ix >= 0) & (ix < kv.shape[1])).sum())  # noqa: E731
+
+    def run(n):
+        toks = np.sort(rng.choice(w.S, size=n, replace=False))
+        qs, dos, ixs = q[:, toks], do[:, toks], idx[:, toks]
+        o, lse = oracle.sparse_forward(qs, kv, ixs, w.sm_scale, w.Dv)
+        o = inputs.round_to_dtype(o, w.dtype)
+        t0 = time.perf_counter()
+        oracle.sparse_backward(qs, kv, o, dos, lse, ixs, w.sm_scale, w.Dv)
+        return time.perf_counter() - t0, valid(ixs), n
+
+    el, pairs, n = run(16)
+    n = int(min(w.S, max(16, n * budget_s / max(el, 1e-3))))
+    el, pairs, n = run(n)
+    frac = pairs / valid(idx)
+    return (sparse_flops(w, idx) * frac / el / 1e12, el,
+            f"the whole backward (dQ and dKV contributions) of {n} seeded tokens ({pairs} of {valid(idx)} valid "
+            f"(token, slot) pairs) of {w.name}, {el:.1f} s of float64 numpy, extrapolated by pairs")
 
 
 # ------------------------------------------------------------------ main
@@ -436,22 +536,26 @@ def run_reference(args):
         return 0
     from attention_backward_gb300 import inputs
 
-    w = inputs.WORKLOADS[MAIN_WORKLOAD]
+    w = inputs.WORKLOADS[args.workload]
     vals, els = [], []
+    desc = ""
     for i in range(args.warmup + args.steps):
-        v_, el, nh = cpu_oracle_sample(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+        v_, el, desc = cpu_oracle_sample(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
         if i >= args.warmup:
             vals.append(v_)
             els.append(el)
     value = float(np.mean(vals))
     cores = os.cpu_count()
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+    unit = "TFLOP/s"
+    work = sparse_flops(w, inputs.sparse_inputs(w)[3]) if w.kind == "sparse" else dense_flops(w)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(els)) * 1e3,
+            "ms_per_step_extrapolated": work / (value * 1e12) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": MAIN_WORKLOAD, "B": w.B, "S": w.S, "H": w.HQ, "D": w.D, "causal": True},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{nh} of {w.HQ} query heads, both batch rows, per step"},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
@@ -500,6 +604,8 @@ def describe(w, r, pk, pk_kind, world=1):
     out["roofline"] = roof
     out["stages_ms"] = {"preprocess": r["ms_pre"], "main": ms_main, "land": r["ms_land"]}
     out["ms_per_step"] = ms
+    out["ms_per_step_pct"] = r["ms_step_pct"]
+    out["main_ms_pct"] = r["ms_main_pct"]
     return out, flops
 
 
@@ -557,7 +663,7 @@ def main():
         "metric": METRIC, "value": d["value"], "unit": d["unit"], "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w),
-        "roofline": d["roofline"], "stages_ms": d["stages_ms"],
+        "ms_per_step_pct": r["ms_step_pct"], "roofline": d["roofline"], "stages_ms": d["stages_ms"],
     }
     if w.kind == "sparse":
         line["TFLOP/s"] = d["TFLOP/s"]
@@ -573,12 +679,10 @@ def main():
     del r
     torch.cuda.empty_cache()
     if not args.no_extra and world == 1:
-        line["workloads"] = extra_workloads(w.name, max(5, args.steps // 2), args.warmup, device, pk, pk_kind)
-    if not args.no_cpu and world == 1 and rank == 0 and w.kind == "dense":
-        cv, el, nh = cpu_oracle_sample(w)
-        line["cpu_baseline"] = {"value": cv, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": f"{nh} of {w.HQ} query heads x {w.B} batch rows of {w.name}, "
-                                          f"{el:.1f} s of float64 numpy"}
+        line["workloads"] = extra_workloads(w.name, max(5, args.steps // 2), args.warmup, device, pk, pk_kind,
+                                            cpu=not args.no_cpu)
+    if not args.no_cpu and world == 1 and rank == 0:
+        line["cpu_baseline"] = cpu_baseline_entry(w)
     else:
         line["cpu_baseline"] = None
     if rank == 0:
@@ -591,8 +695,16 @@ def main():
     return 0
 
 
-def extra_workloads(main_name, steps, warmup, device, pk, pk_kind):
-    """The other workloads, same timing method, each with its own roofline."""
+def cpu_baseline_entry(w):
+    """The oracle timed on this host's cores on a bounded sample of ``w``."""
+    cv, el, desc = cpu_oracle_sample(w)
+    return {"value": cv, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle", "sample": desc,
+            "extrapolated": "whole heads" not in desc}
+
+
+def extra_workloads(main_name, steps, warmup, device, pk, pk_kind, cpu=True):
+    """The other workloads, same timing method, each with its own roofline and,
+    with ``cpu``, the oracle timed beside it on a bounded sample."""
     import torch
 
     from attention_backward_gb300 import inputs
@@ -603,9 +715,11 @@ def extra_workloads(main_name, steps, warmup, device, pk, pk_kind):
             continue
         r = (time_sparse if w.kind == "sparse" else time_dense)(w, steps, warmup, device)
         d, _ = describe(w, r, pk, pk_kind)
-        out[name] = d
         del r
         torch.cuda.empty_cache()
+        d["config"] = workload_config(w)
+        d["cpu_baseline"] = cpu_baseline_entry(w) if cpu else None
+        out[name] = d
     return out
 
 

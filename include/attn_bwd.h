@@ -39,9 +39,13 @@
  *     ATTN_ERR_UNSUPPORTED, never as a silent fallback.  Faults found by the
  *     kernels themselves (a bounded wait that ran out) are recorded in the
  *     workspace and reported by attn_bwd_check_error.
- *   - Order on one stream, same workspace: attn_bwd_preprocess, then
- *     attn_bwd / attn_bwd_gqa (or attn_bwd_sparse), then attn_bwd_dq_land
- *     (or attn_bwd_sparse_land).
+ *   - One call per backward: attn_bwd / attn_bwd_gqa (dense) and
+ *     attn_bwd_sparse (top-k) take Q, K, V, O, dO and the LSE, validate every
+ *     argument, then queue the three launches on ``stream`` and deliver dQ,
+ *     dK and dV (or dQ and dKV).  The launches are also exported one by one
+ *     (the split form): attn_bwd_preprocess, then attn_bwd_gqa_main (or
+ *     attn_bwd_sparse_main), then attn_bwd_dq_land (or attn_bwd_sparse_land),
+ *     on one stream with the same workspace.
  */
 #ifndef ATTN_BWD_H_
 #define ATTN_BWD_H_
@@ -84,7 +88,13 @@ typedef struct {
  *   causal != 0                     : j <= i  (the page's "cols <= rows"),
  *   window_left = W > 0             : i - W < j <= i  (implies causal).
  * cu_seqlens: device int32 [num_seqs + 1], non-decreasing from 0 and ending
- * at most at S (the kernels clamp to S); NULL for dense batches. */
+ * at most at S (the kernels clamp to S); NULL for dense batches.  Rows past
+ * cu_seqlens[num_seqs] belong to no sequence: the kernels never use their Q,
+ * K, V, dO, O or LSE values as operands (tiles that overhang them are zeroed
+ * in shared memory after the load), so they may hold anything, NaN included;
+ * dQ rows there are written as zero and dK/dV rows there are not written.
+ * No longest-sequence length is needed: the persistent kernels compute the
+ * tile count of every sequence on the device. */
 typedef struct {
   int32_t causal;
   int32_t window_left;
@@ -98,7 +108,7 @@ typedef struct {
  * (0 for dense).  Every region is 256-byte aligned. */
 ATTN_BWD_API size_t attn_bwd_workspace_size(int64_t B, int64_t S, int64_t H, int64_t Dq, int64_t dkv_elems);
 
-/* Launch 1: delta_i = sum_d O_id dO_id (f32), LSE*log2(e), zeroed dQ (and
+/* Split form, launch 1: delta_i = sum_d O_id dO_id (f32), LSE*log2(e), zeroed dQ (and
  * dKV) accumulators, cleared error word and tile counter.  The delta row
  * preprocess of the TileOPs page ("delta_rows" in its Base and Tiled
  * programs).
@@ -111,62 +121,114 @@ ATTN_BWD_API attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so,
                                   int64_t Dv, int64_t Dq, int64_t dkv_elems, attn_dtype_t dtype, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
-/* Launch 2, grouped-query attention: one CTA per (key tile of 128 rows,
- * KV head, batch) keeps K and V in shared memory and dK, dV in tensor memory,
- * loops over the G = HQ/HKV query heads of its group and their query blocks,
- * writes dK (times sm_scale) and dV once in the input dtype and adds its dQ
- * partials into the workspace accumulator.  Query head h reads KV head h / G.
- *   q, dO  : [B,S,HQ,D] 16-bit;  k, v, dk, dv : [B,S,HKV,D] 16-bit (dk, dv written)
- *   D in {64, 128};  G in {1, 2, 4, 8, 16};  S >= 1;  B == 1 when varlen. */
-ATTN_BWD_API attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
-                           attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S,
-                           int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
-                           const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
-                           void* workspace, size_t workspace_bytes, void* stream);
+/* Group sizes G = HQ / HKV the dense path accepts: at most 16 query heads per
+ * KV head in fp16 and at most 8 in bf16.  P is rounded to the input dtype
+ * before dV += P^T dO (as the TileOPs page's "Tiled" program does); with bf16's
+ * 8-bit significand the rounding errors of one key row, summed over more than
+ * 8 heads of short causal rows, exceed the bf16 tolerance, so larger groups
+ * are refused (ATTN_ERR_UNSUPPORTED) rather than served inexactly. */
+#define ATTN_BWD_MAX_GROUP_F16 16
+#define ATTN_BWD_MAX_GROUP_BF16 8
 
-/* Launch 2, multi-head attention: attn_bwd_gqa with HQ == HKV == H (the
- * page's MHA op is GQA with H_kv = H). */
+/* The whole dense backward of grouped-query attention in one call: the
+ * TileOPs page's three launches behind one op call ("Summary": preprocess,
+ * main kernel, dQ landing), queued on ``stream`` after every argument has
+ * been checked, so a call either queues all three or nothing.
+ *   q, o, dO, dq : [B,S,HQ,D] 16-bit;  k, v, dk, dv : [B,S,HKV,D] 16-bit;
+ *   lse : f32 natural-log LSE [B,HQ,S] of the forward with strides slse
+ *   (b, s, h);  dq, dk, dv are written (dK and dV once per key row by their
+ *   owning CTA, dQ = sm_scale * the f32 sum of its partials).
+ *   D in {64, 128};  G = HQ / HKV within the limits above;  S >= 1;  B == 1
+ *   when varlen;  sm_scale finite.  Query head h reads KV head h / G.
+ *   workspace : at least attn_bwd_workspace_size(B, S, HQ, D, 0) bytes,
+ *   16-byte aligned, owned by the caller; its contents on entry do not matter.
+ * Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, bad stride, size
+ * or mask), ATTN_ERR_UNSUPPORTED (head dim, group size, dtype, sizes past
+ * 2^31 rows), ATTN_ERR_WORKSPACE, all before anything is queued;
+ * ATTN_ERR_LAUNCH if the runtime refuses a launch. */
+ATTN_BWD_API attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
+                                        const void* v, attn_strides_t sv, const void* o, attn_strides_t so,
+                                        const void* dO, attn_strides_t sdo, const float* lse, attn_strides_t slse,
+                                        int64_t B, int64_t S, int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype,
+                                        float sm_scale, const attn_mask_t* mask, void* dq, attn_strides_t sdq,
+                                        void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/* Multi-head attention: attn_bwd_gqa with HQ == HKV == H (the page's MHA op is
+ * GQA with H_kv = H). */
 ATTN_BWD_API attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
-                       attn_strides_t sv, const void* dO, attn_strides_t sdo, int64_t B, int64_t S, int64_t H,
-                       int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dk,
-                       attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace, size_t workspace_bytes,
-                       void* stream);
+                                    attn_strides_t sv, const void* o, attn_strides_t so, const void* dO,
+                                    attn_strides_t sdo, const float* lse, attn_strides_t slse, int64_t B, int64_t S,
+                                    int64_t H, int64_t D, attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask,
+                                    void* dq, attn_strides_t sdq, void* dk, attn_strides_t sdk, void* dv,
+                                    attn_strides_t sdv, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Launch 3: dQ = cast(sm_scale * dQacc), the TileOPs page's "dq_land".
+/* Split form, launch 2 of the dense path: one CTA per (key tile of 128 rows,
+ * KV head, batch) keeps K and V in shared memory and dK, dV in tensor memory,
+ * loops over the G query heads of its group and their query blocks, writes dK
+ * (times sm_scale) and dV once in the input dtype and adds its dQ partials
+ * into the workspace accumulator (the "Tiled" program's placement; KV-head
+ * ownership as in the flash-linear-attention issue, "Bounded scope" items
+ * 1-2).  Arguments as for attn_bwd_gqa; needs attn_bwd_preprocess first and
+ * attn_bwd_dq_land after it, on the same stream and workspace. */
+ATTN_BWD_API attn_status_t attn_bwd_gqa_main(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
+                                             const void* v, attn_strides_t sv, const void* dO, attn_strides_t sdo,
+                                             int64_t B, int64_t S, int64_t HQ, int64_t HKV, int64_t D,
+                                             attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* dk,
+                                             attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace,
+                                             size_t workspace_bytes, void* stream);
+
+/* Split form, launch 3 of the dense path: dQ = cast(sm_scale * dQacc), the
+ * TileOPs page's "dq_land".
  *   dq : [B,S,H,D] 16-bit (written).  B*S*H below 2^31, else
  *   ATTN_ERR_UNSUPPORTED. */
 ATTN_BWD_API attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
                                attn_dtype_t dtype, float sm_scale, const void* workspace, size_t workspace_bytes,
                                void* stream);
 
-/* Launch 2, top-k sparse attention over shared latent rows (the tilelang
- * sparse MLA backward): query t of batch b, head h (KV head g = h / (H/HKV))
- * attends the latent rows kv[b, idx[b,t,g,s], g, :] for every slot s whose
- * index lies in [0, SKV); other entries (-1 pads) are not visible.  K is the
- * whole DQK-wide row, V its first DV columns.  One CTA owns a (token, KV
- * head) pair with all of its query heads, so dQ (which already includes
- * sm_scale) is written here, once; dKV = dK + [dV, 0] partials are added into
- * the workspace's f32 dKV accumulator, which attn_bwd_sparse_land casts.
- * The preprocess before it runs with Dq = 0 (no dQ accumulator) and
- * dkv_elems = B*SKV*HKV*DQK.
- *   q, dq : [B,S,H,DQK];  kv : [B,SKV,HKV,DQK] stored densely (row stride
- *   DQK); dO : [B,S,H,DV] 16-bit
- *   idx : int32 [B,S,HKV,topk] with strides sidx (slot stride 1)
- *   DQK = 576, DV = 512;  G = H / HKV <= 64;  topk >= 1.  A group of G < 64
- *   heads (a tensor-parallel split of the heads) is computed padded to 64 heads
- *   whose extra rows contribute exactly zero, so it takes 64/G times the work
- *   of its own heads. */
+/* The whole top-k sparse backward over shared latent rows (the tilelang
+ * sparse MLA backward) in one call: the preprocess (delta, LSE*log2(e), a
+ * zeroed f32 dKV accumulator; no dQ accumulator), the sparse kernel and the
+ * dKV cast, queued on ``stream`` after every argument has been checked.
+ * Query t of batch b, head h (KV head g = h / (H/HKV)) attends the latent rows
+ * kv[b, idx[b,t,g,s], g, :] for every slot s whose index lies in [0, SKV);
+ * other entries (-1 pads) are not visible.  K is the whole DQK-wide row, V its
+ * first DV columns, and dKV = dK + [dV, 0].
+ *   q, dq : [B,S,H,DQK];  kv, dkv : [B,SKV,HKV,DQK], kv stored densely (row
+ *   stride DQK);  o, dO : [B,S,H,DV] 16-bit;  lse : f32 [B,H,S] with strides
+ *   slse (b, s, h);  idx : int32 [B,S,HKV,topk] with strides sidx (slot
+ *   stride 1);  DQK = 576, DV = 512;  G = H / HKV <= 64;  topk >= 1.
+ *   workspace : attn_bwd_workspace_size(B, S, H, 0, B*SKV*HKV*DQK) bytes.
+ * A group of G < 64 heads (a tensor-parallel split of the heads) is computed
+ * padded to 64 heads whose extra rows contribute exactly zero, so it takes
+ * 64/G times the work of its own heads.  Errors as for attn_bwd_gqa. */
 ATTN_BWD_API attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
-                                           const void* dO, attn_strides_t sdo, const int32_t* idx,
+                                           const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
+                                           const float* lse, attn_strides_t slse, const int32_t* idx,
                                            attn_strides_t sidx, int64_t B, int64_t S, int64_t SKV, int64_t H,
                                            int64_t HKV, int64_t DQK, int64_t DV, int64_t topk, attn_dtype_t dtype,
-                                           float sm_scale, void* dq, attn_strides_t sdq, void* workspace,
-                                           size_t workspace_bytes, void* stream);
+                                           float sm_scale, void* dq, attn_strides_t sdq, void* dkv,
+                                           attn_strides_t sdkv, void* workspace, size_t workspace_bytes,
+                                           void* stream);
 
-/* Launch 3 of the sparse path: dKV = cast(dKVacc) (the sparse kernel applies
- * sm_scale to dS itself: dKV mixes the scaled dK term with the unscaled dV
- * term, so the scale cannot be folded into a landing pass as on the dense
- * path).  B, S, H locate the workspace regions as at preprocess time.
+/* Split form, launch 2 of the sparse path: one CTA owns a (token, KV head)
+ * pair with all of its query heads, so dQ (which already includes sm_scale)
+ * is written here, once; dKV partials are added into the workspace's f32 dKV
+ * accumulator, which attn_bwd_sparse_land casts.  The preprocess before it
+ * runs with Dq = 0 (no dQ accumulator) and dkv_elems = B*SKV*HKV*DQK.
+ * Arguments as for attn_bwd_sparse. */
+ATTN_BWD_API attn_status_t attn_bwd_sparse_main(const void* q, attn_strides_t sq, const void* kv, attn_strides_t skv,
+                                                const void* dO, attn_strides_t sdo, const int32_t* idx,
+                                                attn_strides_t sidx, int64_t B, int64_t S, int64_t SKV, int64_t H,
+                                                int64_t HKV, int64_t DQK, int64_t DV, int64_t topk,
+                                                attn_dtype_t dtype, float sm_scale, void* dq, attn_strides_t sdq,
+                                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Split form, launch 3 of the sparse path: dKV = cast(dKVacc) (the sparse
+ * kernel applies sm_scale to dS itself: dKV mixes the scaled dK term with the
+ * unscaled dV term, so the scale cannot be folded into a landing pass as on
+ * the dense path).  B, S, H locate the workspace regions as at preprocess
+ * time.
  *   dkv : [B,SKV,HKV,DQK] 16-bit (written).  B*SKV*HKV below 2^31, else
  *   ATTN_ERR_UNSUPPORTED. */
 ATTN_BWD_API attn_status_t attn_bwd_sparse_land(void* dkv, attn_strides_t sdkv, int64_t B, int64_t S, int64_t SKV,
@@ -213,28 +275,30 @@ ATTN_BWD_API attn_status_t attn_bwd_selftest_timeout(void* workspace, size_t wor
 /* Size of the library-held workspace of attn_bwd_gqa_noalloc (32 MiB). */
 #define ATTN_BWD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
-/* The whole dense backward (attn_bwd_preprocess, attn_bwd_gqa and
- * attn_bwd_dq_land on ``stream``) for callers that cannot allocate device
- * memory: plugins running inside a framework that owns all device memory
- * through its own pool, and latency-critical loops that cannot afford the
- * device-wide synchronisation of cudaMalloc/cudaFree.  This entry point is a
- * convenience of this library; the pages it follows have no counterpart.
+/* The whole dense backward (attn_bwd_gqa's three launches on ``stream``) for
+ * callers that cannot allocate device memory: plugins running inside a
+ * framework that owns all device memory through its own pool, and
+ * latency-critical loops that cannot afford the device-wide synchronisation
+ * of cudaMalloc/cudaFree.  This entry point is a convenience of this library;
+ * the pages it follows have no counterpart.
  *
  * Instead of a workspace argument it uses one device array of
  * ATTN_BWD_NOALLOC_SCRATCH_BYTES that the library holds, on every GPU that
  * loads it, until the process exits; it allocates nothing.  Problems whose
  * attn_bwd_workspace_size(B, S, HQ, D, 0) exceeds that size are rejected with
- * ATTN_ERR_WORKSPACE before anything is queued.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  All calls on a
+ * ATTN_ERR_WORKSPACE, and every other argument is checked as attn_bwd_gqa
+ * checks it, before anything is queued.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture, and do not use this entry point across a device reset
+ * (cudaDeviceReset), after which the kept address is stale.  All calls on a
  * device share the array: calls whose work overlaps on the GPU (different
  * streams, or several host threads) race and corrupt each other's results, so
  * serialise them.  The preprocess clears what must start at zero, so earlier
- * calls' leftovers do not matter.  attn_bwd_check_error cannot inspect this
- * array; a kernel fault is still reported by CUDA at the next synchronisation.
- *   q, o, dO, dq : [B,S,HQ,D];  k, v, dk, dv : [B,S,HKV,D] (16-bit);
- *   lse : f32 [B,HQ,S] (natural log) with strides slse (b, s, h);
- *   the other arguments as for attn_bwd_preprocess / attn_bwd_gqa. */
+ * calls' leftovers do not matter.  Errors found by the kernels themselves (a
+ * bounded wait that ran out) are recorded in the array; read them with
+ * attn_bwd_noalloc_check_error.
+ *   Arguments as for attn_bwd_gqa, without the workspace. */
 ATTN_BWD_API attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
                                                 const void* v, attn_strides_t sv, const void* o, attn_strides_t so,
                                                 const void* dO, attn_strides_t sdo, const float* lse,
@@ -242,6 +306,12 @@ ATTN_BWD_API attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq
                                                 int64_t D, attn_dtype_t dtype, float sm_scale,
                                                 const attn_mask_t* mask, void* dq, attn_strides_t sdq, void* dk,
                                                 attn_strides_t sdk, void* dv, attn_strides_t sdv, void* stream);
+
+/* attn_bwd_check_error for the array of attn_bwd_gqa_noalloc on the current
+ * device: synchronises ``stream`` and reports ATTN_OK, ATTN_ERR_TIMEOUT (with
+ * the site code in *device_code, if not NULL) or ATTN_ERR_DEVICE.  The next
+ * attn_bwd_gqa_noalloc call on the device clears the recorded error. */
+ATTN_BWD_API attn_status_t attn_bwd_noalloc_check_error(void* stream, int32_t* device_code);
 
 /* Device scratch bytes that attn_bwd_gqa_host needs to process the problem
  * in ``chunks`` chunks of KV heads (0 for an invalid shape). */
@@ -255,8 +325,8 @@ ATTN_BWD_API size_t attn_bwd_host_scratch_size(int64_t B, int64_t S, int64_t HQ,
  * The problem is split into ceil(HKV / ceil(HKV / chunks)) chunks of KV heads;
  * a chunk and its query heads are independent of the others.  Each chunk is
  * copied in (strided head slices of the host tensors into contiguous device
- * buffers, on ``copy_in_stream``), run through attn_bwd_preprocess,
- * attn_bwd_gqa and attn_bwd_dq_land (on ``stream``) and copied out (on
+ * buffers, on ``copy_in_stream``), run through attn_bwd_gqa (its three
+ * launches, on ``stream``) and copied out (on
  * ``copy_out_stream``), with two buffer slots so that copies of neighbouring
  * chunks overlap the kernels.  The copies start after the work queued on
  * ``stream`` before the call, and ``stream`` waits for the last copy-out, so

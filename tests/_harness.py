@@ -48,8 +48,9 @@ def sample_rows(S, n, seed, block=128, cu=None):
     return np.array(sorted(rows))
 
 
-def run_dense(w, problem, poison=True, workspace=None, stream=None):
-    """The three launches through the binding; outputs pre-filled with NaN so
+def run_dense(w, problem, poison=True, workspace=None, stream=None, split=False):
+    """The dense backward through the C ABI: the one-call attn_bwd_gqa, or with
+    ``split`` its three launches one by one; outputs pre-filled with NaN so
     that any element the kernels fail to write shows up."""
     import torch
 
@@ -68,9 +69,12 @@ def run_dense(w, problem, poison=True, workspace=None, stream=None):
     ws = workspace if workspace is not None else ab._binding.new_workspace(w.B, w.S, w.HQ, w.D)
     if poison and workspace is None:
         ws.fill_(0xFF)
-    ab.preprocess(to, tdo, tl, ws, Dq=w.D, stream=stream)
-    ab.attn_bwd_gqa(tq, tk, tv, tdo, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
-    ab.dq_land(dq, ws, w.sm_scale, stream)
+    if split:
+        ab.preprocess(to, tdo, tl, ws, Dq=w.D, stream=stream)
+        ab.gqa_main(tq, tk, tv, tdo, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
+        ab.dq_land(dq, ws, w.sm_scale, stream)
+    else:
+        ab.attn_bwd_gqa(tq, tk, tv, to, tdo, tl, dq, dk, dv, ws, w.sm_scale, w.causal, w.window, cu, stream)
     ab.check_error(ws, stream)
     return dq, dk, dv, ws
 
@@ -108,8 +112,9 @@ def sparse_problem(w, idx_override=None):
     return q, kv, do, idx, o, np.ascontiguousarray(lse, dtype=np.float32)
 
 
-def run_sparse(w, problem, poison=True):
-    """The sparse path's three launches through the binding, outputs NaN-poisoned."""
+def run_sparse(w, problem, poison=True, split=False):
+    """The sparse path through the C ABI (the one-call attn_bwd_sparse, or its
+    three launches with ``split``), outputs NaN-poisoned."""
     import torch
 
     import attention_backward_gb300 as ab
@@ -129,8 +134,38 @@ def run_sparse(w, problem, poison=True):
     fill = float("nan") if poison else 0.0
     dq = torch.full_like(tq, fill)
     dkv = torch.full_like(tkv, fill)
-    ab.preprocess(to, tdo, tl, ws, Dq=0, dkv_elems=dkv_elems)
-    ab.attn_bwd_sparse(tq, tkv, tdo, tidx, dq, ws, w.sm_scale, w.Dv)
-    ab.sparse_land(dkv, ws, B, S, H)
+    if split:
+        ab.preprocess(to, tdo, tl, ws, Dq=0, dkv_elems=dkv_elems)
+        ab.sparse_main(tq, tkv, tdo, tidx, dq, ws, w.sm_scale, w.Dv)
+        ab.sparse_land(dkv, ws, B, S, H)
+    else:
+        ab.attn_bwd_sparse(tq, tkv, to, tdo, tl, tidx, dq, dkv, ws, w.sm_scale, w.Dv)
     ab.check_error(ws)
     return dq, dkv
+
+
+def oracle_rows_chunked(problem, w, q_rows=None, k_rows=None, heads=None, chunk=1024):
+    """The oracle's dQ rows ``q_rows`` and dK/dV rows ``k_rows`` (positions
+    along S; None: none), evaluated ``chunk`` positions per call so that no
+    call holds more than chunk x sequence-length score matrices; rows not
+    asked for are NaN.  ``heads`` restricts the query heads as in
+    oracle.backward (dK/dV rows of KV heads without a listed query head come
+    back as zero)."""
+    q, k, v, o, do, lse = problem
+    out = None
+    for which in ("q", "k"):
+        rows = q_rows if which == "q" else k_rows
+        if rows is None:
+            continue
+        rows = np.asarray(rows)
+        for c0 in range(0, rows.size, chunk):
+            r = rows[c0:c0 + chunk]
+            part = oracle.backward(q, k, v, o, do, lse, w.sm_scale, heads=heads, **mask_of(w),
+                                   **({"q_rows": r} if which == "q" else {"k_rows": r}))
+            if out is None:
+                out = [a.copy() for a in part]
+            else:
+                for a, b in zip(out, part):
+                    m = ~np.isnan(b)
+                    a[m] = b[m]
+    return out

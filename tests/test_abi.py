@@ -122,49 +122,147 @@ def test_tile_schedule_rejects_bad_sizes(ab):
 
 
 def test_argument_errors_return_before_any_launch(ab):
+    """The split-form launches reject bad calls with a status and queue nothing
+    (the fake pointers are 16-byte aligned and never dereferenced)."""
     lib = ab.library()
     S = ab._binding.Strides
     z = S(0, 0, 0)
     good = S(2048 * 32 * 128, 32 * 128, 128)
     m = ab._binding.Mask(1, -1, None, 0)
-    # null pointers
-    assert lib.attn_bwd_gqa(None, good, None, good, None, good, None, good, 2, 2048, 32, 32, 128, 0, 0.1,
-                            ctypes.byref(m), None, good, None, good, None, 0, None) == 1
-    fake = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
-    # unsupported head dim
-    assert lib.attn_bwd_gqa(fake, good, fake, good, fake, good, fake, good, 2, 2048, 32, 32, 96, 0, 0.1,
-                            ctypes.byref(m), fake, good, fake, good, fake, 1 << 30, None) == 2
-    # HQ not a multiple of HKV
-    assert lib.attn_bwd_gqa(fake, good, fake, good, fake, good, fake, good, 2, 2048, 6, 4, 128, 0, 0.1,
-                            ctypes.byref(m), fake, good, fake, good, fake, 1 << 30, None) == 1
-    # misaligned pointer
-    assert lib.attn_bwd_gqa(fake + 2, good, fake, good, fake, good, fake, good, 2, 2048, 32, 32, 128, 0, 0.1,
-                            ctypes.byref(m), fake, good, fake, good, fake, 1 << 30, None) == 1
-    # zero strides
-    assert lib.attn_bwd_gqa(fake, z, fake, good, fake, good, fake, good, 2, 2048, 32, 32, 128, 0, 0.1,
-                            ctypes.byref(m), fake, good, fake, good, fake, 1 << 30, None) == 1
-    # workspace too small
-    assert lib.attn_bwd_gqa(fake, good, fake, good, fake, good, fake, good, 2, 2048, 32, 32, 128, 0, 0.1,
-                            ctypes.byref(m), fake, good, fake, good, fake, 1024, None) == 3
-    # window of zero, varlen with B > 1
-    m0 = ab._binding.Mask(1, 0, None, 0)
-    assert lib.attn_bwd_gqa(fake, good, fake, good, fake, good, fake, good, 2, 2048, 32, 32, 128, 0, 0.1,
-                            ctypes.byref(m0), fake, good, fake, good, fake, 1 << 30, None) == 1
-    mv = ab._binding.Mask(1, -1, fake, 3)
-    assert lib.attn_bwd_gqa(fake, good, fake, good, fake, good, fake, good, 2, 2048, 32, 32, 128, 0, 0.1,
-                            ctypes.byref(mv), fake, good, fake, good, fake, 1 << 30, None) == 1
+    fake = 1 << 20
+
+    def main(q=fake, sq=good, B=2, H=32, HKV=32, D=128, dtype=0, scale=0.1, mask=m, ws_bytes=1 << 30):
+        return lib.attn_bwd_gqa_main(q, sq, fake, good, fake, good, fake, good, B, 2048, H, HKV, D, dtype, scale,
+                                     ctypes.byref(mask), fake, good, fake, good, fake, ws_bytes, None)
+
+    assert lib.attn_bwd_gqa_main(None, good, None, good, None, good, None, good, 2, 2048, 32, 32, 128, 0, 0.1,
+                                 ctypes.byref(m), None, good, None, good, None, 0, None) == 1   # null pointers
+    assert main(D=96) == 2                                 # unsupported head dim
+    assert main(H=6, HKV=4) == 1                           # HQ not a multiple of HKV
+    assert main(q=fake + 2) == 1                           # misaligned pointer
+    assert main(sq=z) == 1                                 # zero strides
+    assert main(ws_bytes=1024) == 3                        # workspace too small
+    assert main(mask=ab._binding.Mask(1, 0, None, 0)) == 1            # window of zero
+    assert main(mask=ab._binding.Mask(1, -1, fake, 3)) == 1           # varlen with B > 1
+    assert main(scale=float("nan")) == 1
+    # group sizes beyond the precision limits: 16 heads per KV head in fp16, 8 in bf16
+    assert main(H=32, HKV=1) == 2
+    assert main(H=16, HKV=1, dtype=1) == 2
     # preprocess: bad head dim, workspace too small
     assert lib.attn_bwd_preprocess(fake, good, fake, good, fake, S(64, 1, 2048), 2, 2048, 32, 12, 128, 0, 0,
                                    fake, 1 << 30, None) == 1
     assert lib.attn_bwd_preprocess(fake, good, fake, good, fake, S(64, 1, 2048), 2, 2048, 32, 128, 128, 0, 0,
                                    fake, 4096, None) == 3
-    # landing: unsupported dtype code
+    # landing: unsupported dtype code, non-finite scale
     assert lib.attn_bwd_dq_land(fake, good, 2, 2048, 32, 128, 7, 0.1, fake, 1 << 30, None) == 2
+    assert lib.attn_bwd_dq_land(fake, good, 2, 2048, 32, 128, 0, float("inf"), fake, 1 << 30, None) == 1
+
+
+def _one_call_args(ab, **kw):
+    """Arguments of attn_bwd_gqa / attn_bwd_gqa_noalloc for a 2x2048x32x128
+    problem, with fake (never dereferenced) pointers; keywords override."""
+    S = ab._binding.Strides
+    fake = 1 << 20
+    a = dict(q=fake, sq=S(2048 * 32 * 128, 32 * 128, 128), o=fake, lse=fake, slse=S(32 * 2048, 1, 2048),
+             dq=fake, dk=fake, B=2, S=2048, HQ=32, HKV=32, D=128, dtype=0, scale=0.1,
+             mask=ab._binding.Mask(1, -1, None, 0), ws=fake, ws_bytes=1 << 32)
+    a.update(kw)
+    return a
+
+
+def _gqa(ab, **kw):
+    a = _one_call_args(ab, **kw)
+    f = 1 << 20
+    sq = a["sq"]
+    return ab.library().attn_bwd_gqa(a["q"], sq, f, sq, f, sq, a["o"], sq, f, sq, a["lse"], a["slse"], a["B"],
+                                     a["S"], a["HQ"], a["HKV"], a["D"], a["dtype"], a["scale"],
+                                     ctypes.byref(a["mask"]), a["dq"], sq, a["dk"], sq, f, sq, a["ws"],
+                                     a["ws_bytes"], None)
+
+
+def _noalloc(ab, **kw):
+    a = _one_call_args(ab, **kw)
+    f = 1 << 20
+    sq = a["sq"]
+    return ab.library().attn_bwd_gqa_noalloc(a["q"], sq, f, sq, f, sq, a["o"], sq, f, sq, a["lse"], a["slse"],
+                                             a["B"], a["S"], a["HQ"], a["HKV"], a["D"], a["dtype"], a["scale"],
+                                             ctypes.byref(a["mask"]), a["dq"], sq, a["dk"], sq, f, sq, None)
+
+
+BAD_CALLS = [
+    # (name, overrides, status): 1 invalid argument, 2 unsupported, 3 workspace
+    ("null q", dict(q=None), 1),
+    ("null o", dict(o=None), 1),
+    ("null lse", dict(lse=None), 1),
+    ("null dq", dict(dq=None), 1),
+    ("misaligned q", dict(q=(1 << 20) + 2), 1),
+    ("misaligned dq", dict(dq=(1 << 20) + 8), 1),
+    ("misaligned lse", dict(lse=(1 << 20) + 2), 1),
+    ("odd stride", dict(sq=None), 1),
+    ("HQ % HKV", dict(HQ=6, HKV=4), 1),
+    ("window 0", dict(mask=None), 1),
+    ("window -2", dict(mask="w-2"), 1),
+    ("varlen B > 1", dict(mask="varlen"), 1),
+    ("varlen no sequences", dict(mask="varlen0", B=1), 1),
+    ("NaN scale", dict(scale=float("nan")), 1),
+    ("infinite scale", dict(scale=float("inf")), 1),
+    ("head dim 96", dict(D=96), 2),
+    ("dtype 7", dict(dtype=7), 2),
+    ("G = 32 fp16", dict(HQ=32, HKV=1), 2),
+    ("G = 16 bf16", dict(HQ=32, HKV=2, dtype=1), 2),
+]
+
+
+def _resolve(ab, kw):
+    S, M = ab._binding.Strides, ab._binding.Mask
+    kw = dict(kw)
+    if "sq" in kw and kw["sq"] is None:
+        kw["sq"] = S(2048 * 32 * 128, 32 * 128 + 4, 128)  # 8-byte head stride: not a 16-byte multiple
+    if "mask" in kw:
+        kw["mask"] = {None: M(1, 0, None, 0), "w-2": M(1, -2, None, 0), "varlen": M(1, -1, 1 << 20, 3),
+                      "varlen0": M(1, -1, 1 << 20, 0)}[kw["mask"]]
+    return kw
+
+
+@pytest.mark.parametrize("name,kw,status", BAD_CALLS, ids=[c[0] for c in BAD_CALLS])
+def test_one_call_forms_reject_before_any_launch(ab, name, kw, status):
+    """attn_bwd_gqa checks every argument of its three launches before it
+    queues the first; attn_bwd_gqa_noalloc makes the same checks before it
+    touches the device (no GPU here: a call that got further would fail
+    differently)."""
+    kw = _resolve(ab, kw)
+    assert _gqa(ab, **kw) == status, name
+    # a problem that fits the library-held 32 MiB workspace
+    assert _noalloc(ab, **{"S": 256, **kw}) == status, name
+
+
+def test_one_call_workspace_and_sparse_checks(ab):
+    lib = ab.library()
+    S = ab._binding.Strides
+    assert _gqa(ab, ws_bytes=4096) == 3
+    assert _gqa(ab, ws=None) == 1
+    fake = 1 << 20
+    sq = S(4096 * 64 * 576, 64 * 576, 576)
+    skv = S(4096 * 576, 576, 576)
+    sdo = S(4096 * 64 * 512, 64 * 512, 512)
+    sidx = S(4096 * 2048, 2048, 2048)
+    sl = S(64 * 4096, 1, 4096)
+
+    def sparse(o=fake, lse=fake, dkv=fake, sdkv=skv, dtype=1, ws_bytes=1 << 40, topk=2048):
+        return lib.attn_bwd_sparse(fake, sq, fake, skv, o, sdo, fake, sdo, lse, sl, fake, sidx, 1, 4096, 4096, 64, 1,
+                                   576, 512, topk, dtype, 0.04, fake, sq, dkv, sdkv, fake, ws_bytes, None)
+
+    assert sparse(o=None) == 1 and sparse(lse=None) == 1 and sparse(dkv=None) == 1
+    assert sparse(dkv=fake + 4) == 1
+    assert sparse(sdkv=S(0, 0, 0)) == 1
+    assert sparse(ws_bytes=4096) == 3
+    assert sparse(topk=0) == 1
+    assert sparse(dtype=5) == 2
 
 
 def test_sparse_argument_errors_return_before_any_launch(ab):
-    """attn_bwd_sparse and its landing pass reject bad calls with a status and
-    queue nothing (the fake pointers below are never dereferenced)."""
+    """attn_bwd_sparse_main and its landing pass reject bad calls with a status
+    and queue nothing (the fake pointers below are never dereferenced)."""
     lib = ab.library()
     S = ab._binding.Strides
     fake = 1 << 20
@@ -175,8 +273,8 @@ def test_sparse_argument_errors_return_before_any_launch(ab):
 
     def call(q=fake, kv=fake, do=fake, idx=fake, dq=fake, ws=fake, B=1, Sq=4096, SKV=4096, H=64, HKV=1, DQK=576,
              DV=512, topk=2048, dtype=1, scale=0.04, skv_=skv, ws_bytes=1 << 40):
-        return lib.attn_bwd_sparse(q, sq, kv, skv_, do, sdo, idx, sidx, B, Sq, SKV, H, HKV, DQK, DV, topk, dtype,
-                                   scale, dq, sq, ws, ws_bytes, None)
+        return lib.attn_bwd_sparse_main(q, sq, kv, skv_, do, sdo, idx, sidx, B, Sq, SKV, H, HKV, DQK, DV, topk,
+                                        dtype, scale, dq, sq, ws, ws_bytes, None)
 
     assert call(q=None) == 1 and call(idx=None) == 1 and call(ws=None) == 1   # null pointers
     assert call(H=64, HKV=3) == 1                                              # H not a multiple of HKV

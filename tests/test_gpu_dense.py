@@ -6,7 +6,7 @@ import pytest
 import oracle
 from attention_backward_gb300 import inputs
 
-from _harness import assert_close, dense_problem, mask_of, run_dense, sample_rows, to_np
+from _harness import assert_close, dense_problem, mask_of, oracle_rows_chunked, run_dense, sample_rows, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -26,13 +26,21 @@ SMALL = [
     inputs.scaled(C1, name="s2_noncausal", S=2, causal=False),
     inputs.scaled(C1, name="s129_bf16", S=129, dtype="bf16"),
     inputs.scaled(C1, name="s127_b3", S=127, B=3, HQ=1, HKV=1),
+    # every group size the ABI accepts, in both dtypes: G in {1, 2, 4, 8, 16} for
+    # fp16 and {1, 2, 4, 8} for bf16, plus group sizes that are not powers of two.
+    # bf16 with G > 8 is refused (test_group_size_limits_are_enforced): the
+    # rounding of P to 16 bits before the dV product (as the page's Tiled
+    # program does) alone exceeds the bf16 tolerance there on short causal rows.
     inputs.scaled(C3, name="gqa_g4_s384", S=384, HQ=8, HKV=2),
-    # G = 16 runs in fp16: in bf16 the rounding of P to 16 bits before the dV
-    # product (the page's Tiled program does the same) alone exceeds the bf16
-    # tolerance at this group size on short causal rows.
     inputs.scaled(C3, name="gqa_g16_s300_causal_f16", S=300, HQ=16, HKV=1, causal=True, dtype="f16"),
     inputs.scaled(C3, name="gqa_g8_s300_causal_bf16", S=300, HQ=8, HKV=1, causal=True),
+    inputs.scaled(C3, name="gqa_g8_s300_causal_f16", S=300, HQ=16, HKV=2, causal=True, dtype="f16"),
+    inputs.scaled(C3, name="gqa_g4_s260_causal_f16", S=260, HQ=8, HKV=2, causal=True, dtype="f16"),
     inputs.scaled(C3, name="gqa_g2_f16_s520", S=520, HQ=4, HKV=2, dtype="f16"),
+    inputs.scaled(C3, name="gqa_g2_s330_causal_bf16", S=330, HQ=4, HKV=2, causal=True),
+    inputs.scaled(C3, name="gqa_g3_s300_causal_bf16", S=300, HQ=6, HKV=2, causal=True),
+    inputs.scaled(C3, name="gqa_g12_s280_causal_f16", S=280, HQ=12, HKV=1, causal=True, dtype="f16"),
+    inputs.scaled(C4, name="gqa_g8_d64_s300_causal_bf16", S=300, HQ=16, HKV=2, window=-1, cu_seqlens=None),
     inputs.scaled(C4, name="varlen_d64_w100", S=700, HQ=4, HKV=2, window=100, cu_seqlens=(0, 33, 161, 390, 700)),
     inputs.scaled(C4, name="varlen_empty_and_single", S=300, HQ=2, HKV=1, window=64,
                   cu_seqlens=(0, 0, 1, 1, 130, 300)),
@@ -58,6 +66,88 @@ def test_small_cases_match_oracle(w):
     assert_close(dq, rq, w, "dq")
     assert_close(dk, rk, w, "dk")
     assert_close(dv, rv, w, "dv")
+
+
+def test_split_launches_match_one_call():
+    """The three launches called one by one (attn_bwd_preprocess,
+    attn_bwd_gqa_main, attn_bwd_dq_land) give the one-call results: the same
+    dK/dV bits, dQ within tolerance of the oracle."""
+    for w in (inputs.scaled(C3, name="split_g4", S=384, HQ=8, HKV=2, causal=True),
+              inputs.scaled(C4, name="split_d64", S=500, HQ=4, HKV=2, window=100, cu_seqlens=(0, 200, 500))):
+        prob = dense_problem(w)
+        a = run_dense(w, prob)
+        b = run_dense(w, prob, split=True)
+        assert (to_np(a[1]) == to_np(b[1])).all() and (to_np(a[2]) == to_np(b[2])).all()
+        q, k, v, o, do, lse = prob
+        rq, _, _ = oracle.backward(q, k, v, o, do, lse, w.sm_scale, **mask_of(w))
+        assert_close(b[0], rq, w, "dq (split launches)")
+
+
+def test_group_size_limits_are_enforced():
+    """Group sizes past the precision limits are refused with
+    ATTN_ERR_UNSUPPORTED before anything runs: bf16 beyond 8 query heads per
+    KV head, fp16 beyond 16."""
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    for dt, hq in ((torch.bfloat16, 16), (torch.float16, 32)):
+        q = torch.zeros(1, 128, hq, 128, dtype=dt, device="cuda")
+        kv = torch.zeros(1, 128, 1, 128, dtype=dt, device="cuda")
+        lse = torch.zeros(1, hq, 128, dtype=torch.float32, device="cuda")
+        with pytest.raises(ab.AttnBwdError, match="unsupported"):
+            ab.backward(q, kv, kv, q, q, lse, 0.1, causal=True)
+
+
+def _poisoned_tail_case(w, tail):
+    """Packed sequences ending ``tail`` rows before S; every input row past the
+    last sequence holds NaN (Q, K, V, O, dO and the LSE)."""
+    import torch
+
+    import attention_backward_gb300 as ab
+    from _harness import torch_dtype
+
+    q, k, v, o, do, lse = dense_problem(w)
+    dt = torch_dtype(w)
+    end = w.cu_seqlens[-1]
+    assert end == w.S - tail
+    t = lambda a: torch.from_numpy(a).cuda().to(dt)  # noqa: E731
+    tq, tk, tv, to, tdo = t(q), t(k), t(v), t(o), t(do)
+    tl = torch.from_numpy(lse).cuda()
+    for x in (tq, tk, tv, to, tdo):
+        x[:, end:] = float("nan")
+    tl[:, :, end:] = float("nan")
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device="cuda")
+    dq, dk, dv = ab.backward(tq, tk, tv, to, tdo, tl, w.sm_scale, w.causal, w.window, cu)
+    torch.cuda.synchronize()
+    return (q, k, v, o, do, lse), dq, dk, dv
+
+
+@pytest.mark.parametrize("w,tail", [
+    # head dim 128: the last sequence ends inside a key tile and a query block,
+    # and a whole 128-row block lies past it
+    (inputs.scaled(C4, name="tail_d128", D=128, Dv=128, S=700, HQ=4, HKV=2, window=-1,
+                   cu_seqlens=(0, 250, 480)), 220),
+    (inputs.scaled(C4, name="tail_d128_noncausal", D=128, Dv=128, S=400, HQ=2, HKV=2, causal=False, window=-1,
+                   cu_seqlens=(0, 150, 301)), 99),
+    # head dim 64 with a window
+    (inputs.scaled(C4, name="tail_d64_w100", S=640, HQ=4, HKV=2, window=100, cu_seqlens=(0, 33, 161, 390)), 250),
+], ids=lambda x: getattr(x, "name", str(x)))
+def test_rows_past_the_last_sequence_may_hold_nan(w, tail):
+    """Rows of a packed batch past cu_seqlens[num_seqs] belong to no sequence:
+    NaN there must not reach any gradient of a row inside a sequence (a zero P
+    or dS times NaN is NaN, so the kernels zero those rows after loading), and
+    the dQ rows there are written as zero."""
+    prob, dq, dk, dv = _poisoned_tail_case(w, tail)
+    q, k, v, o, do, lse = prob
+    end = w.cu_seqlens[-1]
+    rq, rk, rv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, **mask_of(w))
+    # the oracle leaves rows outside every sequence as NaN: they are skipped here
+    assert np.isnan(rq[:, end:]).all() and not np.isnan(rq[:, :end]).any()
+    assert_close(dq, rq, w, "dq")
+    assert_close(dk, rk, w, "dk")
+    assert_close(dv, rv, w, "dv")
+    assert (to_np(dq)[:, end:] == 0).all()
 
 
 def test_single_position_closed_form():
@@ -124,28 +214,9 @@ def test_strided_inputs():
     assert_close(dv, rv, w, "dv")
 
 
-def _full_size(w, n_rows, heads):
-    prob = dense_problem(w)
-    q, k, v, o, do, lse = prob
-    dq, dk, dv, _ = run_dense(w, prob)
-    rows = sample_rows(w.S, n_rows, w.seed, cu=w.cu_seqlens)
-    rq, rk, rv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, q_rows=rows, k_rows=rows, **mask_of(w))
-    assert_close(dq, rq, w, "dq (sampled rows)")
-    assert_close(dk, rk, w, "dk (sampled rows)")
-    assert_close(dv, rv, w, "dv (sampled rows)")
-    if heads:
-        G = w.HQ // w.HKV
-        hq = [h for g in heads for h in range(g * G, (g + 1) * G)]
-        fq, fk, fv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, heads=hq, **mask_of(w))
-        fq[:, :, [h for h in range(w.HQ) if h not in hq]] = np.nan
-        assert_close(dq, fq, w, f"dq (query heads {hq})")
-        sel = np.full(w.HKV, False)
-        sel[heads] = True
-        fk[:, :, ~sel] = np.nan
-        fv[:, :, ~sel] = np.nan
-        assert_close(dk, fk, w, f"dk (kv heads {heads})")
-        assert_close(dv, fv, w, f"dv (kv heads {heads})")
-    # properties that hold on every row: rows of P sum to one and rows of dS to zero
+def _sum_invariants(w, do, dk, dv):
+    """Properties that hold on every row: rows of P sum to one and rows of dS
+    to zero, so per KV head sum_j dV_j = sum_i dO_i and sum_j dK_j = 0."""
     G = w.HQ // w.HKV
     gv, gk = to_np(dv), to_np(dk)
     for b in range(w.B):
@@ -156,16 +227,63 @@ def _full_size(w, n_rows, heads):
             np.testing.assert_allclose(gk[b, :, g].sum(0), 0.0, atol=2e-3 * np.sqrt(n) * 4)
 
 
-def test_workload_mha_causal_2x2048x32x128():
-    _full_size(C2, 256, heads=[0, 31])
+def test_workload_mha_causal_2x2048x32x128_in_full():
+    """Causal MHA 2x2048x32x128 fp16, every element of dQ, dK and dV against
+    the oracle."""
+    w = C2
+    prob = dense_problem(w)
+    q, k, v, o, do, lse = prob
+    dq, dk, dv, _ = run_dense(w, prob)
+    rq, rk, rv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, **mask_of(w))
+    assert_close(dq, rq, w, "dq")
+    assert_close(dk, rk, w, "dk")
+    assert_close(dv, rv, w, "dv")
+    _sum_invariants(w, do, dk, dv)
+
+
+def test_workload_varlen_window_in_full():
+    """Packed sliding-window GQA (4 sequences, 16384 tokens, window 1024, D 64
+    bf16), every element against the oracle (evaluated 1024 rows at a time)."""
+    w = C4
+    prob = dense_problem(w)
+    dq, dk, dv, _ = run_dense(w, prob)
+    every = np.arange(w.S)
+    rq, rk, rv = oracle_rows_chunked(prob, w, q_rows=every, k_rows=every)
+    assert_close(dq, rq, w, "dq")
+    assert_close(dk, rk, w, "dk")
+    assert_close(dv, rv, w, "dv")
+    _sum_invariants(w, prob[4], dk, dv)
 
 
 def test_workload_gqa_16384():
-    _full_size(C3, 384, heads=None)
-
-
-def test_workload_varlen_window():
-    _full_size(C4, 512, heads=[0, 7])
+    """Unmasked GQA 1x16384, HQ 32 / HKV 4, D 128 bf16: every dQ row of query
+    heads 0 and 31, every dK/dV row of KV heads 0 and 3, and 512 seeded rows
+    (plus every tile edge) of every head."""
+    w = C3
+    prob = dense_problem(w)
+    q, k, v, o, do, lse = prob
+    dq, dk, dv, _ = run_dense(w, prob)
+    rows = sample_rows(w.S, 512, w.seed)
+    rq, rk, rv = oracle_rows_chunked(prob, w, q_rows=rows, k_rows=rows)
+    assert_close(dq, rq, w, "dq (seeded rows, every head)")
+    assert_close(dk, rk, w, "dk (seeded rows, every KV head)")
+    assert_close(dv, rv, w, "dv (seeded rows, every KV head)")
+    G = w.HQ // w.HKV
+    every = np.arange(w.S)
+    for g, hq in ((0, 0), (w.HKV - 1, w.HQ - 1)):
+        fq, _, _ = oracle_rows_chunked(prob, w, q_rows=every, heads=[hq], chunk=512)
+        keep = np.full(w.HQ, False)
+        keep[hq] = True
+        fq[:, :, ~keep] = np.nan
+        assert_close(dq, fq, w, f"dq (query head {hq}, every row)")
+        _, fk, fv = oracle_rows_chunked(prob, w, k_rows=every, heads=list(range(g * G, (g + 1) * G)), chunk=512)
+        kv_keep = np.full(w.HKV, False)
+        kv_keep[g] = True
+        fk[:, :, ~kv_keep] = np.nan
+        fv[:, :, ~kv_keep] = np.nan
+        assert_close(dk, fk, w, f"dk (KV head {g}, every row)")
+        assert_close(dv, fv, w, f"dv (KV head {g}, every row)")
+    _sum_invariants(w, do, dk, dv)
 
 
 def test_workload_mha_causal_1x256_in_full():

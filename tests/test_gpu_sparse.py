@@ -35,6 +35,20 @@ def test_small_sparse_cases_match_oracle(w):
     assert_close(dkv, rkv, w, "dkv")
 
 
+def test_sparse_split_launches_match_one_call():
+    """attn_bwd_preprocess, attn_bwd_sparse_main and attn_bwd_sparse_land one
+    by one give what the one-call attn_bwd_sparse gives (dQ is written once per
+    token: the same bits; dKV within tolerance of the oracle)."""
+    w = inputs.scaled(C5, name="split_s200", S=200, topk=128)
+    prob = sparse_problem(w)
+    q, kv, do, idx, o, lse = prob
+    a = run_sparse(w, prob)
+    b = run_sparse(w, prob, split=True)
+    assert (to_np(a[0]) == to_np(b[0])).all()
+    _, rkv = oracle.sparse_backward(q, kv, o, do, lse, idx, w.sm_scale, w.Dv)
+    assert_close(b[1], rkv, w, "dkv (split launches)")
+
+
 def test_sparse_edge_index_lists():
     """Repeated indices count as separate slots, out-of-range indices and -1
     are not visible, and a token with no visible slot gets dQ = 0."""
@@ -56,14 +70,17 @@ def test_sparse_edge_index_lists():
 
 
 def test_sparse_workload_4096_sampled():
-    """The full sparse workload: dQ of sampled tokens and dKV of sampled rows
+    """The full sparse workload: dQ of 512 seeded tokens and dKV of 512 seeded
+    latent rows (plus every 128-row tile edge and the rows 0, 1, 2047, 2048,
+    4095, where the index lists change from full prefixes to sampled sets)
     against the oracle, and the column sums of dKV on every row."""
     w = C5
     prob = sparse_problem(w)
     q, kv, do, idx, o, lse = prob
     dq, dkv = run_sparse(w, prob)
-    toks = sample_rows(w.S, 48, w.seed)
-    rows = sample_rows(w.S, 48, w.seed + 1)
+    edge = [0, 1, 2047, 2048, w.S - 1]
+    toks = np.union1d(sample_rows(w.S, 512, w.seed), edge)
+    rows = np.union1d(sample_rows(w.S, 512, w.seed + 1), edge)
     rq, _ = oracle.sparse_backward(q, kv, o, do, lse, idx, w.sm_scale, w.Dv, tokens=toks)
     _, rkv = oracle.sparse_backward(q, kv, o, do, lse, idx, w.sm_scale, w.Dv, kv_rows=rows)
     assert_close(dq, rq, w, "dq (sampled tokens)")

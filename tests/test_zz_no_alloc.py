@@ -51,6 +51,10 @@ def test_noalloc_matches_workspace_entry_points_twice(w):
         assert_close(dv, rv, w, f"dv (call {call})")
         # dK and dV are written once by their owning CTA: the same bits as the reference
         assert (to_np(dk) == rk).all() and (to_np(dv) == rv).all()
+    # no kernel recorded an error in the library-held workspace
+    code = ctypes.c_int32(-1)
+    assert ab.library().attn_bwd_noalloc_check_error(None, ctypes.byref(code)) == 0
+    assert code.value == 0
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
