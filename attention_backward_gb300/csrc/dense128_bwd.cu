@@ -34,15 +34,18 @@
 // go back to the producer separately, each as soon as the reduces of its own
 // two staging slabs have read it.
 //
-// Warp roles (14 warps): 0-3 dQ epilogue (lane = query; at the end of a tile
+// Warp roles (16 warps): 0-3 dQ epilogue (lane = query; at the end of a tile
 // they also land dK/dV, lane = key row, while the softmax warps start the next
 // one), 4-11 two warpgroups of softmax/dS work (each owns 64 of the 128 query
-// columns of all 128 key rows), 12 TMA producer, 13 MMA issuer.  A stage, a
+// columns of all 128 key rows), 12 TMA producer, 13 MMA issuer, 14-15 idle
+// (they complete the fourth warpgroup of the register split).  A stage, a
 // TMEM region or the dS tile is reused only after an mbarrier shows that its
 // last reader is done.  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+// the register split below needs the bounded waits' slow paths inlined
+#define AB_INLINE_WAITS 1
 #include "common.cuh"
 #include "cvt.cuh"
 #include "dense_common.cuh"
@@ -87,7 +90,15 @@ constexpr int T_S = 0;     // S^T f32; P^T pairs at 0-63, dS^T pairs at 64-127
 constexpr int T_DP = 128;  // dP^T f32, then the step's dQ f32 [128 queries x 128 d]
 constexpr int T_DV = 256;
 constexpr int T_DK = 384;
-constexpr int THREADS = 14 * 32;
+// 16 warps in four warpgroups, launched at 128 registers each (the whole
+// register file: 16 warps x 32 lanes x 128 = 65536) and re-split at entry:
+// the softmax warpgroups take 168 so that a warp keeps both halves of its
+// S^T / dP^T columns in flight next to P, the epilogue keeps 104 and the
+// producer/MMA warpgroup 72.  Each sub-partition holds one warp of every
+// warpgroup: 32 x (104 + 168 + 168 + 72) = 16384 registers, its whole file.
+constexpr int THREADS = 16 * 32;
+constexpr uint32_t REG_EPI = 104, REG_SOFT = 168, REG_CTL = 72;
+static_assert(REG_EPI + 2 * REG_SOFT + REG_CTL == 4 * 128, "register split must equal the launch's registers");
 
 // Each stage has two halves with their own barriers: Q (with the step's LSE2
 // and delta) and dO.  The f32 dQ staging of a step covers both halves, and
@@ -178,7 +189,27 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
-  if (warp == 12) {
+  // Every role ends here: all warps meet, then the MMA warp releases TMEM.
+  // Each role runs it at its own end (and returns), so that no code is shared
+  // between roles that run under different register budgets.
+  auto finish = [&]() {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+    if (warp == 13) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+  };
+  // each role sets its register budget at its own entry, so that the
+  // compiler sees one budget along every path through a role
+  if (warp >= 14) {
+    // two spare warps of the control warpgroup: nothing to do until teardown
+    setmaxnreg_dec<REG_CTL>();
+    finish();
+    return;
+  } else if (warp == 12) {
+    setmaxnreg_dec<REG_CTL>();
     // ============================================================ producer
     int pend_full[ST], pend_d[ST];
 #pragma unroll
@@ -332,7 +363,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (pend_d[i] >= 0) mbar_drain(&bars[FULLD0 + i], pend_d[i]);
       }
     }
+    finish();
+    return;
   } else if (warp == 13) {
+    setmaxnreg_dec<REG_CTL>();
     // ============================================================ MMA issuer (whole warp, one elected lane)
     constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, BN, false, false);
     constexpr uint32_t IDESC_KV = idesc_f16(BF16, 128, D, false, true);
@@ -416,8 +450,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     mma_commit_w(&bars[DRAIN]);
     if (lane == 0) mbar_drain(&bars[DRAIN], 0);
     __syncwarp();
+    finish();
+    return;
   } else if (warp >= 4) {
-    // ============================================================ softmax / dS, dK / dV landing
+    setmaxnreg_inc<REG_SOFT>();
+    // ============================================================ softmax / dS
     const int wg = (warp - 4) >> 2, quad = warp & 3;
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -451,34 +488,33 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
         if (!(ok = mbar_wait_warp(&bars[S_FULL], gs & 1, wc, kErrWaitS))) break;
         tc_fence_after();
+        // both 32-column halves of this warpgroup's S^T in flight at once, then P
+        // in place (LSE2 four columns at a time, so that only the S^T/P values stay live)
+        uint32_t sr[HALF];
+        tmem_ld32(sb + wg * HALF, sr);
+        tmem_ld32(sb + wg * HALF + 32, sr + 32);
+        tmem_ld_wait();
+        if (full_vis) {
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(sb + wg * HALF + ch * 32, r);
-          tmem_ld_wait();
-          // LSE2 four columns at a time, so that only r and pv stay live
-          if (full_vis) {
+          for (int c4 = 0; c4 < HALF / 4; ++c4) {
+            const float4 t = lse4[c4];
+            const float l4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 t = lse4[ch * 8 + c4];
-              const float l4[4] = {t.x, t.y, t.z, t.w};
+            for (int e = 0; e < 4; ++e)
+              pv[4 * c4 + e] = ex2(fmaf(__uint_as_float(sr[4 * c4 + e]), p.scale_log2, -l4[e]));
+          }
+        } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pv[ch * 32 + 4 * c4 + e] = ex2(fmaf(__uint_as_float(r[4 * c4 + e]), p.scale_log2, -l4[e]));
-            }
-          } else {
+          for (int c4 = 0; c4 < HALF / 4; ++c4) {
+            const float4 t = lse4[c4];
+            const float l4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 t = lse4[ch * 8 + c4];
-              const float l4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 4 * c4 + e, cc = ch * 32 + c, q = qc0 + cc;
-                bool vis = kvalid && q < ti.len;
-                if (cm) vis = vis && kpos <= q;
-                if (W > 0) vis = vis && q < kpos + W;
-                pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -l4[e])) : 0.f;
-              }
+            for (int e = 0; e < 4; ++e) {
+              const int cc = 4 * c4 + e, q = qc0 + cc;
+              bool vis = kvalid && q < ti.len;
+              if (cm) vis = vis && kpos <= q;
+              if (W > 0) vis = vis && q < kpos + W;
+              pv[cc] = vis ? ex2(fmaf(__uint_as_float(sr[cc]), p.scale_log2, -l4[e])) : 0.f;
             }
           }
         }
@@ -501,19 +537,22 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DS_SFREE], (gs - 1) & 1, wc, kErrWaitDSFree))) break;
         tc_fence_after();
         uint8_t* dsb = sm + OFF_DS + wg * DS_BLOCK;
+        // both halves of this warpgroup's dP^T columns in flight at once
+        uint32_t dr[HALF];
+        tmem_ld32(tmem + lane_off + T_DP + wg * HALF, dr);
+        tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
+        tmem_ld_wait();
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + T_DP + wg * HALF + ch * 32, r);
-          tmem_ld_wait();
           uint32_t dsw[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
+          for (int c = 0; c < 32; c += 4) {
             const int cc = ch * 32 + c;
-            const float2 dl = reinterpret_cast<const float2*>(dlt4)[cc / 2];  // delta of columns cc, cc + 1
-            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dl.x);
-            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dl.y);
-            dsw[c / 2] = pack2<BF16>(d0, d1);
+            const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
+            dsw[c / 2] = pack2<BF16>(pv[cc] * (__uint_as_float(dr[cc]) - dl.x),
+                                     pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y));
+            dsw[c / 2 + 1] = pack2<BF16>(pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z),
+                                         pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w));
           }
           // dS^T pairs into the second half of this warpgroup's S^T columns, and dS
           // as the MN-major A operand of dQ: 64-query block wg, row = key, 16-byte chunks 4ch..4ch+3
@@ -531,7 +570,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       }
       if (!ok) break;
     }
+    finish();
+    return;
   } else {
+    setmaxnreg_dec<REG_EPI>();
     // ============================================================ dQ epilogue (lane = query)
     const int quad = warp;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -648,15 +690,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       }
     }
     if (leader) bulk_wait_all();
-  }
 
-  // ---------------------------------------------------------------- teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 13) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    finish();
   }
 }
 

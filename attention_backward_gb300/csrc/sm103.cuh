@@ -66,8 +66,19 @@ __device__ __forceinline__ void raise_error(const WaitCtx& c, int code) {
   atomicCAS(c.err, 0, code);
 }
 
+// The slow paths below are called functions by default (they keep the
+// inline fast path of every wait small).  A kernel that re-splits its
+// registers per warpgroup (setmaxnreg) defines AB_INLINE_WAITS before
+// including this header: a called function would have to fit the register
+// budget of every role that calls it, and the compiler refuses that.
+#if defined(AB_INLINE_WAITS)
+#define AB_WAIT_SLOW_FN __forceinline__
+#else
+#define AB_WAIT_SLOW_FN __noinline__
+#endif
+
 // Slow path of mbar_wait: bounded polling with abort and error checks.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
+static __device__ AB_WAIT_SLOW_FN bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& c, int code) {
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
@@ -104,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
 
 // Last-resort drain used on the abort path: waits (bounded, without consulting
 // the abort flag) for a phase whose producer is known to be in flight.
-static __device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+static __device__ AB_WAIT_SLOW_FN void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
   while (!mbar_try(bar, parity)) {
     if (global_ns() - t0 > kWaitTimeoutNs) return;
@@ -176,6 +187,20 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // async-proxy (TMA / tensor core) reads.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- register split
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the
+// same call).  The launch provides the registers every warp started with; the
+// warpgroups that shrink must give back at least what the growing ones take,
+// or the growing ones wait.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- tcgen05
