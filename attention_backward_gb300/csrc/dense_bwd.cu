@@ -37,13 +37,16 @@
 // the workspace that the preprocess zeroes; each CTA's producer publishes the
 // tile to the other roles through a two-slot ring in shared memory.
 //
-// Warp roles (14 warps): 0-3 dQ epilogue (TMEM -> shared -> bulk reduce),
+// Warp roles (16 warps): 0-3 dQ epilogue (TMEM -> shared -> bulk reduce),
 // 4-11 two warpgroups of softmax/dS work (each owns half of the BN query
 // columns of all 128 key rows) that also land dK/dV, 12 TMA producer,
-// 13 MMA issuer (one elected thread).  Every wait is bounded.
+// 13 MMA issuer (one elected thread), 14-15 idle (they complete the fourth
+// warpgroup of the register split).  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+// the register split below needs the bounded waits' slow paths inlined
+#define AB_INLINE_WAITS 1
 #include "common.cuh"
 #include "cvt.cuh"
 #include "dense_common.cuh"
@@ -94,7 +97,15 @@ struct Cfg {
   // dQ [128 q x 64 d] goes into the first 64 columns of its step's S^T buffer
   // once dK has read that buffer
   static_assert(3 * BN + 2 * D <= 512, "TMEM budget");
-  static constexpr int THREADS = 14 * 32;
+  // 16 warps in four warpgroups, launched at 128 registers each (the whole
+  // register file) and re-split at entry: the softmax warpgroups take 168 so
+  // that a warp keeps both halves of its S^T / dP^T columns in flight next to
+  // P, the epilogue keeps 104 and the producer/MMA warpgroup 72.  Each
+  // sub-partition holds one warp of every warpgroup: 32 x (104 + 168 + 168 +
+  // 72) = 16384 registers, its whole file.
+  static constexpr int THREADS = 16 * 32;
+  static constexpr uint32_t REG_EPI = 104, REG_SOFT = 168, REG_CTL = 72;
+  static_assert(REG_EPI + 2 * REG_SOFT + REG_CTL == 4 * 128, "register split must equal the launch's registers");
 };
 
 enum Bar : int {
@@ -180,7 +191,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
-  if (warp == 12) {
+  // Every role ends here: all warps meet, then the MMA warp releases TMEM.
+  // Each role runs it at its own end (and returns), so that no code is shared
+  // between roles that run under different register budgets.
+  auto finish = [&]() {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(C::THREADS) : "memory");
+    if (warp == 13) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+  };
+  // each role sets its register budget at its own entry
+  if (warp >= 14) {
+    // two spare warps of the control warpgroup: nothing to do until teardown
+    setmaxnreg_dec<C::REG_CTL>();
+    finish();
+    return;
+  } else if (warp == 12) {
+    setmaxnreg_dec<C::REG_CTL>();
     // ============================================================ producer
     int pend_full[ST];
 #pragma unroll
@@ -318,7 +348,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       for (int i = 0; i < ST; ++i)
         if (pend_full[i] >= 0) mbar_drain(&bars[FULL0 + i], pend_full[i]);
     }
+    finish();
+    return;
   } else if (warp == 13) {
+    setmaxnreg_dec<C::REG_CTL>();
     // ============================================================ MMA issuer
     // The whole warp runs this role with warp-uniform values; one elected lane
     // issues each tcgen05 instruction.
@@ -447,7 +480,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mma_commit_w(&bars[DRAIN]);
     if (lane == 0) mbar_drain(&bars[DRAIN], 0);
     __syncwarp();
+    finish();
+    return;
   } else if (warp >= 4) {
+    setmaxnreg_inc<C::REG_SOFT>();
     // ============================================================ softmax / dS, dK / dV landing
     const int wg = (warp - 4) >> 2, quad = warp & 3;
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
@@ -482,34 +518,32 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
         if (!(ok = mbar_wait_warp(&bars[S_FULL0 + (gs & 1)], (gs >> 1) & 1, wc, kErrWaitS))) break;
         tc_fence_after();
+        // both 32-column halves of this warpgroup's S^T in flight at once, then P
+        uint32_t sr[HALF];
+        tmem_ld32(sb + wg * HALF, sr);
+        tmem_ld32(sb + wg * HALF + 32, sr + 32);
+        tmem_ld_wait();
+        if (full_vis) {
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(sb + wg * HALF + ch * 32, r);
-          tmem_ld_wait();
-          // LSE2 four columns at a time, so that only r and pv stay live
-          if (full_vis) {
+          for (int c4 = 0; c4 < HALF / 4; ++c4) {
+            const float4 t = lse4[c4];
+            const float l4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 t = lse4[ch * 8 + c4];
-              const float l4[4] = {t.x, t.y, t.z, t.w};
+            for (int e = 0; e < 4; ++e)
+              pv[4 * c4 + e] = ex2(fmaf(__uint_as_float(sr[4 * c4 + e]), p.scale_log2, -l4[e]));
+          }
+        } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pv[ch * 32 + 4 * c4 + e] = ex2(fmaf(__uint_as_float(r[4 * c4 + e]), p.scale_log2, -l4[e]));
-            }
-          } else {
+          for (int c4 = 0; c4 < HALF / 4; ++c4) {
+            const float4 t = lse4[c4];
+            const float l4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 t = lse4[ch * 8 + c4];
-              const float l4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 4 * c4 + e, cc = ch * 32 + c, q = qc0 + cc;
-                bool vis = kvalid && q < ti.len;
-                if (cm) vis = vis && kpos <= q;
-                if (W > 0) vis = vis && q < kpos + W;
-                pv[cc] = vis ? ex2(fmaf(__uint_as_float(r[c]), p.scale_log2, -l4[e])) : 0.f;
-              }
+            for (int e = 0; e < 4; ++e) {
+              const int cc = 4 * c4 + e, q = qc0 + cc;
+              bool vis = kvalid && q < ti.len;
+              if (cm) vis = vis && kpos <= q;
+              if (W > 0) vis = vis && q < kpos + W;
+              pv[cc] = vis ? ex2(fmaf(__uint_as_float(sr[cc]), p.scale_log2, -l4[e])) : 0.f;
             }
           }
         }
@@ -533,31 +567,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             !(ok = mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree)))
           break;
         tc_fence_after();
-        // each 32-query chunk of dS is stored as soon as it is computed, so only
-        // one chunk of packed pairs is live next to P
+        // both halves of this warpgroup's dP^T columns in flight at once; the next
+        // step's dP^T may overwrite them as soon as they are loaded
+        uint32_t dr[HALF];
+        tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF, dr);
+        tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + 32, dr + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[DP_FREE]);
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + ch * 32, r);
-          float dlt[32];
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 t = dlt4[ch * 8 + c4];
-            dlt[4 * c4] = t.x, dlt[4 * c4 + 1] = t.y, dlt[4 * c4 + 2] = t.z, dlt[4 * c4 + 3] = t.w;
-          }
-          tmem_ld_wait();
-          if (ch == NCH - 1) {  // dP^T fully loaded: the next step's dP^T may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[DP_FREE]);
-          }
           uint32_t dsw[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
+          for (int c = 0; c < 32; c += 4) {
             const int cc = ch * 32 + c;
-            const float d0 = pv[cc] * (__uint_as_float(r[c]) - dlt[c]);
-            const float d1 = pv[cc + 1] * (__uint_as_float(r[c + 1]) - dlt[c + 1]);
-            dsw[c / 2] = pack2<BF16>(d0, d1);
+            const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
+            dsw[c / 2] = pack2<BF16>(pv[cc] * (__uint_as_float(dr[cc]) - dl.x),
+                                     pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y));
+            dsw[c / 2 + 1] = pack2<BF16>(pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z),
+                                         pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w));
           }
           // dS^T pairs into the second half of this warpgroup's S^T columns
           tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
@@ -613,7 +642,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         }
       }
     }
+    finish();
+    return;
   } else {
+    setmaxnreg_dec<C::REG_EPI>();
     // ============================================================ dQ epilogue
     // The f32 dQ partial of a step is staged in the step's own Q/dO stage (every
     // MMA reading the stage was issued before dQ, so it has completed once
@@ -678,15 +710,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       }
     }
     if (leader && issued) bulk_wait_all();
-  }
-
-  // ---------------------------------------------------------------- teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 13) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    finish();
   }
 }
 

@@ -260,15 +260,25 @@ def gpu_sparse_inputs(w, device):
 
 def _timed_steps(step, steps, warmup, device, stream, ws, nev, flush_bytes, world):
     """W untimed steps, then K steps each bracketed by CUDA events on the
-    launching stream, L2 flushed (a write larger than L2) before each; a barrier
-    and a device synchronisation on both sides of the timed region."""
+    launching stream, L2 flushed before each (a write larger than L2, read back
+    so that no dirty line is left); a barrier and a device synchronisation on
+    both sides of the timed region."""
     import torch
 
     import attention_backward_gb300 as ab
 
     flush = torch.empty(flush_bytes, dtype=torch.uint8, device=device)
-    for _ in range(warmup):
+
+    def clear_l2():
+        # a write larger than L2 evicts the previous step's lines; reading the
+        # buffer back then writes the flush's own dirty lines back to HBM here,
+        # outside the timed region, so every step starts from a cold L2 that
+        # holds no dirty line
         flush.zero_()
+        flush.sum()
+
+    for _ in range(warmup):
+        clear_l2()
         step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
     ab.check_error(ws, stream)
     torch.cuda.synchronize(device)
@@ -279,7 +289,7 @@ def _timed_steps(step, steps, warmup, device, stream, ws, nev, flush_bytes, worl
     torch.cuda.synchronize(device)
     per = []
     for _ in range(steps):
-        flush.zero_()
+        clear_l2()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
         step(ev)
         per.append(ev)
@@ -618,7 +628,8 @@ def workload_config(w):
         c["window"] = w.window
     if w.cu_seqlens is not None:
         c["cu_seqlens"] = list(w.cu_seqlens)
-    c["l2"] = "flushed before every step (256 MiB write)"
+    c["l2"] = ("flushed before every step: a 256 MiB write, then a read of the same buffer, so the step starts "
+               "from a cold L2 that holds no dirty line")
     c["timed"] = "preprocess + main + landing per step"
     return c
 
