@@ -127,7 +127,6 @@ enum Bar : int {
   DKV_FREE,
   DRAIN,
   DP_FREE,
-  DK_DONE,
   TAIL,             // the producer's own: loads of tiles that overhang the last packed sequence
   NUM_BARS
 };
@@ -177,7 +176,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[DKV_FREE], 8);
     mbar_init(&bars[DRAIN], 1);
     mbar_init(&bars[DP_FREE], 8);
-    mbar_init(&bars[DK_DONE], 1);
     mbar_init(&bars[TAIL], 1);
     fence_mbar_init();
   }
@@ -454,9 +452,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_w(tmem + C::T_DK, sb + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + qo + sdesc_step(kk * 2048),
                    IDESC_KV, j > 0 || kk > 0);
-        // dQ overwrites this step's S^T buffer: dV and dK must have read it
-        mma_commit_w(&bars[DK_DONE]);
-        if (!(ok = mbar_wait_warp(&bars[DK_DONE], cur & 1, wc, kErrWaitSFree))) break;
+        // dQ overwrites this step's S^T buffer, which dV and dK read: MMAs issued
+        // by one thread run in issue order, so no wait is needed in between
         const uint32_t dq_cols = sb;
         // one dQ in flight: the epilogue has read the previous one
         if (cur >= 1 && !(ok = mbar_wait_warp(&bars[DQ_EMPTY], (cur - 1) & 1, wc, kErrWaitDQEmpty))) break;
