@@ -37,11 +37,11 @@
 // the workspace that the preprocess zeroes; each CTA's producer publishes the
 // tile to the other roles through a two-slot ring in shared memory.
 //
-// Warp roles (16 warps): 0-3 dQ epilogue (TMEM -> shared -> bulk reduce),
+// Warp roles (16 warps): 0-3 dQ epilogue (TMEM -> shared-memory staging),
 // 4-11 two warpgroups of softmax/dS work (each owns half of the BN query
 // columns of all 128 key rows) that also land dK/dV, 12 TMA producer,
-// 13 MMA issuer (one elected thread), 14-15 idle (they complete the fourth
-// warpgroup of the register split).  Every wait is bounded.
+// 13 MMA issuer (one elected thread), 14 dQ reduce issuer, 15 idle (it
+// completes the fourth warpgroup of the register split).  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -57,14 +57,19 @@ namespace ab {
 
 namespace {
 
+// Q/dO stages and dS tiles in shared memory.  The f32 dQ partial of a step is
+// staged in the step's own Q/dO stage once its MMAs are done, so a stage stays
+// busy until the step's reduce-adds have read it; four stages cover that
+// lifetime, paid for with a single dS tile.
+constexpr int kStages64 = 4;
+constexpr int kDsTiles64 = 1;
+
 template <int D>
 struct Cfg {
   static_assert(D == 64, "head dim 128 runs the kernel of dense128_bwd.cu");
   static constexpr int BM = kDenseBM;
   static constexpr int BN = kDenseBN;
-  // The f32 dQ partial of a step is staged in the step's own Q/dO stage once
-  // its MMAs are done, which leaves room for a second dS tile.
-  static constexpr int STAGES = 3;  // the barrier layout below holds up to 3
+  static constexpr int STAGES = kStages64;
   static constexpr int PREFETCH = 8;  // L2 prefetch distance of Q/dO/LSE/delta, in steps
   static constexpr int NSLAB = D / 64;  // 64-column (128-byte) slabs per row
   static constexpr int KV_SLAB = BM * 128;
@@ -72,7 +77,7 @@ struct Cfg {
   static constexpr int Q_SLAB = BN * 128;
   static constexpr int Q_TILE = Q_SLAB * NSLAB;
   static constexpr int DS_BYTES = BM * BN * 2;
-  static constexpr int NDS = 2;  // dS tiles in shared memory (double-buffered)
+  static constexpr int NDS = kDsTiles64;  // dS tiles in shared memory
   static_assert(BN * D * 4 == 2 * Q_TILE, "the f32 dQ staging of a step fills a Q/dO stage");
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
@@ -84,7 +89,7 @@ struct Cfg {
   static constexpr int OFF_DELTA = OFF_LSE + STAGES * BN * 4;
   static constexpr int OFF_RING = OFF_DELTA + STAGES * BN * 4;
   static constexpr int OFF_BAR = OFF_RING + 64;
-  static constexpr int NBAR = 32;
+  static constexpr int NBAR = 40;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -109,28 +114,28 @@ struct Cfg {
 };
 
 enum Bar : int {
-  FULL0 = 0,        // 3 stages
-  EMPTY0 = 3,       // 3 stages: every reader of the stage is done
-  KV_FULL = 6,
+  FULL0 = 0,                        // kStages64 stages: Q/dO loaded (+ the producer's LSE/delta arrival)
+  EMPTY0 = FULL0 + kStages64,       // ... every reader of the stage is done
+  KV_FULL = EMPTY0 + kStages64,
   KV_FREE,
-  TILE_FULL0 = 8,   // 2 slots
-  TILE_EMPTY0 = 10, // 2 slots
-  S_FULL0 = 12,     // 2 buffers
-  P_READY0 = 14,    // 2 buffers
-  DP_FULL = 16,
+  TILE_FULL0,                       // 2 slots
+  TILE_EMPTY0 = TILE_FULL0 + 2,     // 2 slots
+  S_FULL0 = TILE_EMPTY0 + 2,        // 2 buffers
+  P_READY0 = S_FULL0 + 2,           // 2 buffers
+  DP_FULL = P_READY0 + 2,
   DS_READY,
-  DS_SFREE0,        // 2 dS tiles
-  DQ_FULL = DS_SFREE0 + 2,
+  DS_SFREE0,                        // kDsTiles64 dS tiles: the dQ MMAs have read them
+  DQ_FULL = DS_SFREE0 + kDsTiles64,
   DQ_EMPTY,
-  STG_FULL,         // 4 epilogue warps wrote their staging rows
-  DKV_FULL,
+  STG_FULL0,                        // kStages64 stages: 4 epilogue warps wrote the step's staging rows
+  DKV_FULL = STG_FULL0 + kStages64,
   DKV_FREE,
   DRAIN,
   DP_FREE,
   TAIL,             // the producer's own: loads of tiles that overhang the last packed sequence
   NUM_BARS
 };
-static_assert(NUM_BARS <= 32, "barrier storage");
+static_assert(NUM_BARS <= Cfg<64>::NBAR, "barrier storage");
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
@@ -160,18 +165,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     mbar_init(&bars[KV_FREE], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[TILE_FULL0 + i], 1);
-      mbar_init(&bars[TILE_EMPTY0 + i], 13);  // MMA thread + 8 compute warps + 4 epilogue warps
+      mbar_init(&bars[TILE_EMPTY0 + i], 14);  // MMA warp, 8 softmax warps, 4 epilogue warps, the reduce warp
       mbar_init(&bars[S_FULL0 + i], 1);
     }
     mbar_init(&bars[P_READY0], 8);
     mbar_init(&bars[P_READY0 + 1], 8);
     mbar_init(&bars[DP_FULL], 1);
     mbar_init(&bars[DS_READY], 8);
-    mbar_init(&bars[DS_SFREE0], 1);
-    mbar_init(&bars[DS_SFREE0 + 1], 1);
+    for (int i = 0; i < C::NDS; ++i) mbar_init(&bars[DS_SFREE0 + i], 1);
     mbar_init(&bars[DQ_FULL], 1);
     mbar_init(&bars[DQ_EMPTY], 4);
-    mbar_init(&bars[STG_FULL], 4);
+    for (int i = 0; i < ST; ++i) mbar_init(&bars[STG_FULL0 + i], 4);
     mbar_init(&bars[DKV_FULL], 1);
     mbar_init(&bars[DKV_FREE], 8);
     mbar_init(&bars[DRAIN], 1);
@@ -203,8 +207,41 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   };
   // each role sets its register budget at its own entry
   if (warp >= 14) {
-    // two spare warps of the control warpgroup: nothing to do until teardown
     setmaxnreg_dec<C::REG_CTL>();
+    if (warp == 14) {
+      // ========================================================== dQ reduce issuer
+      // Adds each step's staged f32 dQ partial into the workspace accumulator
+      // (two bulk tensor reduce-adds) and hands the stage back to the producer
+      // as soon as they have read it.  It waits for the reduce engine in a warp
+      // of its own, so the epilogue warps stage the next step meanwhile.
+      uint32_t gs = 0;
+      bool ok = true, issued = false;
+      for (int tc = 0; ok; ++tc) {
+        const int slot = tc & 1;
+        if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+        const TileInfo ti = ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+        if (!ti.valid) break;
+        const int n = p.G * ti.nq;
+        for (int j = 0; j < n; ++j, ++gs) {
+          const int st = gs % ST;
+          if (!(ok = mbar_wait_warp(&bars[STG_FULL0 + st], (gs / ST) & 1, wc, kErrWaitStage))) break;
+          if (lane == 0) {
+            const int h = ti.g * p.G + j / ti.nq, c2 = ti.seq_start + (ti.qlo + j % ti.nq) * BN;
+            tma_reduce_add_4d(&maps.dq, sm + C::OFF_Q + st * C::Q_TILE, 0, h, c2, ti.b);
+            tma_reduce_add_4d(&maps.dq, sm + C::OFF_DO + st * C::Q_TILE, D / 2, h, c2, ti.b);
+            bulk_commit_group();
+            bulk_wait_read_all();  // the stage may be reloaded once the reduces have read it
+            mbar_arrive(&bars[EMPTY0 + st]);
+          }
+          issued = true;
+          __syncwarp();
+        }
+      }
+      if (lane == 0 && issued) bulk_wait_all();
+    }
+    // warp 15: spare, completes the fourth warpgroup of the register split
     finish();
     return;
   } else if (warp == 12) {
@@ -647,12 +684,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
     // The f32 dQ partial of a step is staged in the step's own Q/dO stage (every
     // MMA reading the stage was issued before dQ, so it has completed once
     // DQ_FULL has), one 128-byte-swizzled [128 q x 32 d] slab in the Q part and
-    // one in the dO part, and the stage is handed back to the producer once the
-    // two bulk tensor reduce-adds have read it.
+    // one in the dO part; the reduce warp adds it into the accumulator.
     const int quad = warp;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const bool leader = warp == 0 && lane == 0;
-    bool issued = false;
     uint32_t gs = 0;
     bool ok = true;
     for (int tc = 0; ok; ++tc) {
@@ -665,7 +699,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
       const int n = p.G * ti.nq;
       for (int j = 0; j < n; ++j, ++gs) {
         const int st = gs % ST;
-        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
         if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
         uint32_t r[64];
@@ -689,24 +722,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[STG_FULL]);
-        bool lok = true;
-        if (leader) {
-          lok = mbar_wait(&bars[STG_FULL], gs & 1, wc, kErrWaitStage);
-          if (lok) {
-            const int c2 = ti.seq_start + q0;
-            tma_reduce_add_4d(&maps.dq, half0, 0, h, c2, ti.b);
-            tma_reduce_add_4d(&maps.dq, half1, D / 2, h, c2, ti.b);
-            bulk_commit_group();
-            bulk_wait_read_all();  // the stage may be reloaded once the reduces have read it
-            mbar_arrive(&bars[EMPTY0 + st]);
-            issued = true;
-          }
-        }
-        if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
+        if (lane == 0) mbar_arrive(&bars[STG_FULL0 + st]);
       }
     }
-    if (leader && issued) bulk_wait_all();
     finish();
   }
 }
