@@ -37,10 +37,10 @@
 // Warp roles (16 warps): 0-3 dQ epilogue (lane = query; at the end of a tile
 // they also land dK/dV, lane = key row, while the softmax warps start the next
 // one), 4-11 two warpgroups of softmax/dS work (each owns 64 of the 128 query
-// columns of all 128 key rows), 12 TMA producer, 13 MMA issuer, 14-15 idle
-// (they complete the fourth warpgroup of the register split).  A stage, a
-// TMEM region or the dS tile is reused only after an mbarrier shows that its
-// last reader is done.  Every wait is bounded.
+// columns of all 128 key rows), 12 TMA producer, 13 MMA issuer, 14 dQ reduce
+// issuer, 15 idle (it completes the fourth warpgroup of the register split).
+// A stage, a TMEM region or the dS tile is reused only after an mbarrier shows
+// that its last reader is done.  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     mbar_init(&bars[KV_FREE], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[TILE_FULL0 + i], 1);
-      mbar_init(&bars[TILE_EMPTY0 + i], 13);  // MMA warp + 8 softmax warps + 4 epilogue warps
+      mbar_init(&bars[TILE_EMPTY0 + i], 14);  // MMA warp, 8 softmax warps, 4 epilogue warps, the reduce warp
     }
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[S_FREE], 1);
@@ -204,8 +204,56 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
   // each role sets its register budget at its own entry, so that the
   // compiler sees one budget along every path through a role
   if (warp >= 14) {
-    // two spare warps of the control warpgroup: nothing to do until teardown
     setmaxnreg_dec<REG_CTL>();
+    if (warp == 14) {
+      // ========================================================== dQ reduce issuer
+      // Adds each step's staged f32 dQ partial into the workspace accumulator,
+      // the Q half's two slabs as soon as they are staged, then the dO half's,
+      // and hands each half of the stage back to the producer as soon as its
+      // reduces have read it.  It waits for the reduce engine in a warp of its
+      // own, so the epilogue warps stage the next step meanwhile.
+      uint32_t gs = 0;
+      bool ok = true, issued = false;
+      for (int tc = 0; ok; ++tc) {
+        const int slot = tc & 1;
+        if (!(ok = mbar_wait_warp(&bars[TILE_FULL0 + slot], (tc >> 1) & 1, wc, kErrWaitTile))) break;
+        const TileInfo ti = ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
+        if (!ti.valid) break;
+        const int n = p.G * ti.nq;
+        for (int j = 0; j < n && ok; ++j, ++gs) {
+          const int st = gs % ST;
+          const int h = ti.g * p.G + j / ti.nq, c2 = ti.seq_start + (ti.qlo + j % ti.nq) * BN;
+          uint8_t* stg = sm + OFF_STAGE + st * STAGE;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!(ok = mbar_wait_warp(&bars[(hf == 0 ? STG_FULL0 : STG_FULLB0) + st], (gs / ST) & 1, wc,
+                                      kErrWaitStage)))
+              break;
+            if (lane == 0) {
+#pragma unroll
+              for (int s2 = 0; s2 < 2; ++s2) {
+                const int s4 = 2 * hf + s2;
+                tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
+              }
+              bulk_commit_group();
+            }
+          }
+          if (!ok) break;
+          if (lane == 0) {
+            bulk_wait_read_1();  // the Q half may be reloaded once its reduces have read it
+            mbar_arrive(&bars[EMPTY0 + st]);
+            bulk_wait_read_all();
+            mbar_arrive(&bars[EMPTYD0 + st]);
+          }
+          issued = true;
+          __syncwarp();
+        }
+      }
+      if (lane == 0 && issued) bulk_wait_all();
+    }
+    // warp 15: spare, completes the fourth warpgroup of the register split
     finish();
     return;
   } else if (warp == 12) {
@@ -578,7 +626,6 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
     const int quad = warp;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int q = quad * 32 + lane;  // query of the block = TMEM lane
-    const bool leader = warp == 0 && lane == 0;
     uint32_t gs = 0;
     bool ok = true;
     for (int tc = 0; ok; ++tc) {
@@ -591,18 +638,15 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       const int n = p.G * ti.nq;
       for (int j = 0; j < n; ++j, ++gs) {
         const int st = gs % ST;
-        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
         // dQ complete (so dV and dK, issued before it, have read this step's stage)
         if (!(ok = mbar_wait_warp(&bars[DQ_FULL], gs & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
         // f32 staging in the stage: four 128-byte-swizzled slabs [128 queries x 32 d],
         // d 0-63 (slabs 0-1) in the Q half and d 64-127 (slabs 2-3) in the dO half.
-        // Each half is written, then added with two reduces as one bulk group, so
-        // the Q half's reduces start before the dO half is staged.
+        // Each half is written and handed to the reduce warp, so the Q half's
+        // reduces start before the dO half is staged.
         uint8_t* stg = sm + OFF_STAGE + st * STAGE;
-        const int c2 = ti.seq_start + q0;
-        bool lok = true;
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[64];
           tmem_ld32(tmem + lane_off + T_DP + 64 * hf, r);
@@ -622,27 +666,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           }
           fence_proxy_async_smem();
           __syncwarp();
-          uint64_t* full = &bars[(hf == 0 ? STG_FULL0 : STG_FULLB0) + st];
-          if (lane == 0) mbar_arrive(full);
-          if (leader && lok) {
-            lok = mbar_wait(full, (gs / ST) & 1, wc, kErrWaitStage);
-            if (lok) {
-#pragma unroll
-              for (int s2 = 0; s2 < 2; ++s2) {
-                const int s4 = 2 * hf + s2;
-                tma_reduce_add_4d(&maps.dq, stg + s4 * STG_SLAB, 32 * s4, h, c2, ti.b);
-              }
-              bulk_commit_group();
-            }
-          }
+          if (lane == 0) mbar_arrive(&bars[(hf == 0 ? STG_FULL0 : STG_FULLB0) + st]);
         }
-        if (leader && lok) {
-          bulk_wait_read_1();  // the Q half may be reloaded once its reduces have read it
-          mbar_arrive(&bars[EMPTY0 + st]);
-          bulk_wait_read_all();
-          mbar_arrive(&bars[EMPTYD0 + st]);
-        }
-        if (warp == 0 && !(ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0)) break;
       }
       if (!ok) break;
       // ---- dK / dV of the tile, once every MMA of the tile has completed: lane =
@@ -689,8 +714,6 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         }
       }
     }
-    if (leader) bulk_wait_all();
-
     finish();
   }
 }
