@@ -162,6 +162,7 @@ class Workload:
     cu_seqlens: Optional[tuple] = None  # packed varlen (B == 1)
     topk: int = 0  # sparse only
     seed: int = 0
+    Sk: int = 0  # key/value length of a dense row when it differs from S (0: S)
 
     @property
     def sm_scale(self) -> float:
@@ -170,6 +171,11 @@ class Workload:
     @property
     def G(self) -> int:
         return self.HQ // self.HKV
+
+    @property
+    def skv(self) -> int:
+        """Key/value rows per batch row."""
+        return self.Sk if self.Sk > 0 else self.S
 
 
 # The five workloads.  Seeds follow "20260000 + k" for workload k.
@@ -193,11 +199,11 @@ T_Q, T_K, T_V, T_DO, T_IDX = 1, 2, 3, 4, 5
 
 
 def dense_inputs(w: Workload):
-    """Q [B,S,HQ,D], K [B,S,HKV,D], V [B,S,HKV,Dv], dO [B,S,HQ,Dv] as float32
-    arrays holding values exactly representable in ``w.dtype``."""
+    """Q [B,S,HQ,D], K [B,Sk,HKV,D], V [B,Sk,HKV,Dv], dO [B,S,HQ,Dv] as float32
+    arrays holding values exactly representable in ``w.dtype`` (Sk = w.skv)."""
     q = round_to_dtype(normal_f32(w.seed, T_Q, (w.B, w.S, w.HQ, w.D)), w.dtype)
-    k = round_to_dtype(normal_f32(w.seed, T_K, (w.B, w.S, w.HKV, w.D)), w.dtype)
-    v = round_to_dtype(normal_f32(w.seed, T_V, (w.B, w.S, w.HKV, w.Dv)), w.dtype)
+    k = round_to_dtype(normal_f32(w.seed, T_K, (w.B, w.skv, w.HKV, w.D)), w.dtype)
+    v = round_to_dtype(normal_f32(w.seed, T_V, (w.B, w.skv, w.HKV, w.Dv)), w.dtype)
     do = round_to_dtype(normal_f32(w.seed, T_DO, (w.B, w.S, w.HQ, w.Dv)), w.dtype)
     return q, k, v, do
 

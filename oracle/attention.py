@@ -34,6 +34,11 @@ to query position i iff
                                         plain reading: query i sees itself and
                                         the W-1 keys before it)
   * neither:          always.
+When the keys of a (dense) batch row outnumber or fall short of its queries
+(Sk != Sq; the pages define only Sq == Sk), the masks are aligned at the end
+of the row: with off = Sk - Sq, query i stands at key position i + off, so
+causal means j <= i + off and the window i + off - W < j <= i + off.  A query
+with no visible key (i + off < 0) gets P = 0.
 
 Sparse (top-k) attention follows the tilelang pull request "Adaptive threads
 for sparse MLA backward" (sections "Motivation" and "Benchmark"): one latent
@@ -89,10 +94,10 @@ def visible(S: int, causal: bool, window: int, cu_seqlens=None) -> np.ndarray:
     return m
 
 
-def _visible_block(rows: np.ndarray, cols: np.ndarray, causal: bool, window: int) -> np.ndarray:
+def _visible_block(rows: np.ndarray, cols: np.ndarray, causal: bool, window: int, off: int = 0) -> np.ndarray:
     """Visibility of sequence-local query positions ``rows`` to key positions ``cols``
-    (both inside the same sequence)."""
-    li = rows[:, None]
+    (both inside the same sequence; query i stands at key position i + off)."""
+    li = rows[:, None] + off
     lj = cols[None, :]
     m = np.ones((rows.size, cols.size), dtype=bool)
     if causal or window > 0:
@@ -102,13 +107,26 @@ def _visible_block(rows: np.ndarray, cols: np.ndarray, causal: bool, window: int
     return m
 
 
+def _row_sequences(Sq: int, Sk: int, cu_seqlens):
+    """(query start, query end, key start, key end, off) of every sequence of a
+    batch row: packed sequences share their bounds; a dense row with Sk != Sq
+    aligns its queries with the last Sq key positions."""
+    if cu_seqlens is not None:
+        if Sq != Sk:
+            raise ValueError("packed sequences need equal query and key lengths")
+        return [(a, e, a, e, 0) for (a, e) in sequences(Sq, cu_seqlens)]
+    return [(0, Sq, 0, Sk, Sk - Sq)]
+
+
 # --------------------------------------------------------------------------
 # Dense forward (produces the O and LSE inputs of the backward)
 # --------------------------------------------------------------------------
 
 def forward(q, k, v, scale, causal=False, window=-1, cu_seqlens=None, dtype=np.float32,
             row_chunk=2048):
-    """O [B,S,HQ,Dv] and natural-log LSE [B,HQ,S] of softmax attention.
+    """O [B,S,HQ,Dv] and natural-log LSE [B,HQ,S] of softmax attention over
+    keys k [B,Sk,HKV,D] and values v [B,Sk,HKV,Dv] (Sk = S unless the row is
+    dense; see the module notes on Sk != S).
 
     Rows with no visible key get LSE = -inf and O = 0.
     """
@@ -121,15 +139,15 @@ def forward(q, k, v, scale, causal=False, window=-1, cu_seqlens=None, dtype=np.f
 
     def unit(b, h):
         g = h // G
-        for (a, e) in sequences(S, cu_seqlens):
-            K = k[b, a:e, g, :].astype(dtype)
-            V = v[b, a:e, g, :].astype(dtype)
-            cols = np.arange(e - a)
+        for (a, e, ka, ke, off) in _row_sequences(S, k.shape[1], cu_seqlens):
+            K = k[b, ka:ke, g, :].astype(dtype)
+            V = v[b, ka:ke, g, :].astype(dtype)
+            cols = np.arange(ke - ka)
             for r0 in range(0, e - a, row_chunk):
                 r1 = min(e - a, r0 + row_chunk)
                 Q = q[b, a + r0:a + r1, h, :].astype(dtype)
                 s = (Q @ K.T) * dtype(scale)
-                m = _visible_block(np.arange(r0, r1), cols, causal, window)
+                m = _visible_block(np.arange(r0, r1), cols, causal, window, off)
                 s = np.where(m, s, -np.inf)
                 mx = s.max(axis=1, keepdims=True)
                 mx = np.where(np.isfinite(mx), mx, 0)
@@ -151,49 +169,53 @@ def forward(q, k, v, scale, causal=False, window=-1, cu_seqlens=None, dtype=np.f
 
 def backward(q, k, v, o, do, lse, scale, causal=False, window=-1, cu_seqlens=None,
              q_rows=None, k_rows=None, heads=None):
-    """dQ [B,S,HQ,D], dK [B,S,HKV,D], dV [B,S,HKV,Dv] in float64.
+    """dQ [B,S,HQ,D], dK [B,Sk,HKV,D], dV [B,Sk,HKV,Dv] in float64 (Sk = the key
+    length of k, S unless the row is dense; see the module notes).
 
-    ``q_rows`` / ``k_rows`` (arrays of positions along S) restrict which rows of
-    dQ, respectively of dK and dV, are computed; the others are left as NaN.
-    ``heads`` restricts the query heads visited (dK/dV then sum only those).
-    With both row sets None every row is computed.
+    ``q_rows`` / ``k_rows`` (positions along the query, respectively key,
+    length) restrict which rows of dQ, respectively of dK and dV, are computed;
+    the others are left as NaN.  ``heads`` restricts the query heads visited
+    (dK/dV then sum only those).  With both row sets None every row is computed.
     """
     B, S, HQ, D = q.shape
+    Sk = k.shape[1]
     HKV = k.shape[2]
     G = HQ // HKV
     Dv = v.shape[3]
     full = q_rows is None and k_rows is None
     dq = np.full((B, S, HQ, D), np.nan)
-    dk = np.full((B, S, HKV, D), np.nan)
-    dv = np.full((B, S, HKV, Dv), np.nan)
+    dk = np.full((B, Sk, HKV, D), np.nan)
+    dv = np.full((B, Sk, HKV, Dv), np.nan)
     head_list = list(range(HQ)) if heads is None else list(heads)
     qsel = np.zeros(S, bool) if q_rows is None else np.isin(np.arange(S), q_rows)
-    ksel = np.zeros(S, bool) if k_rows is None else np.isin(np.arange(S), k_rows)
+    ksel = np.zeros(Sk, bool) if k_rows is None else np.isin(np.arange(Sk), k_rows)
     if full:
         qsel[:] = True
         ksel[:] = True
+    seqs = _row_sequences(S, Sk, cu_seqlens)
 
     def unit(b, h):
         g = h // G
         out = []
-        for (a, e) in sequences(S, cu_seqlens):
-            pos = np.arange(e - a)
+        for (a, e, ka, ke, off) in seqs:
+            qpos = np.arange(e - a)
+            kpos = np.arange(ke - ka)
             Qf = q[b, a:e, h, :].astype(np.float64)
-            Kf = k[b, a:e, g, :].astype(np.float64)
-            Vf = v[b, a:e, g, :].astype(np.float64)
+            Kf = k[b, ka:ke, g, :].astype(np.float64)
+            Vf = v[b, ka:ke, g, :].astype(np.float64)
             Of = o[b, a:e, h, :].astype(np.float64)
             dOf = do[b, a:e, h, :].astype(np.float64)
             L = lse[b, h, a:e].astype(np.float64)
             delta = (Of * dOf).sum(axis=1)
             qi = np.nonzero(qsel[a:e])[0]
-            kj = np.nonzero(ksel[a:e])[0]
+            kj = np.nonzero(ksel[ka:ke])[0]
             if full:
-                qi = kj = pos
-            res = {"a": a, "qi": qi, "kj": kj}
+                qi, kj = qpos, kpos
+            res = {"a": a, "ka": ka, "qi": qi, "kj": kj}
             if qi.size:
                 # rows of dQ: every key of the sequence
                 s = scale * (Qf[qi] @ Kf.T)
-                m = _visible_block(qi, pos, causal, window)
+                m = _visible_block(qi, kpos, causal, window, off)
                 P = np.where(m, np.exp(np.where(m, s - L[qi, None], 0.0)), 0.0)
                 dP = dOf[qi] @ Vf.T
                 dS = P * (dP - delta[qi, None]) * scale
@@ -204,7 +226,7 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=-1, cu_seqlens=Non
             if kj.size and not full:
                 # rows of dK and dV: every query of the sequence
                 s = scale * (Qf @ Kf[kj].T)
-                m = _visible_block(pos, kj, causal, window)
+                m = _visible_block(qpos, kj, causal, window, off)
                 P = np.where(m, np.exp(np.where(m, s - L[:, None], 0.0)), 0.0)
                 dP = dOf @ Vf[kj].T
                 dS = P * (dP - delta[:, None]) * scale
@@ -219,18 +241,17 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=-1, cu_seqlens=Non
     # dK/dV of a key/value head: sum over its query heads, in head order
     for b in range(B):
         for g in range(HKV):
-            for (a, e) in sequences(S, cu_seqlens):
-                kj = np.nonzero(ksel[a:e])[0] if not full else np.arange(e - a)
-                dk[b, a + kj, g, :] = 0.0
-                dv[b, a + kj, g, :] = 0.0
+            for (a, e, ka, ke, off) in seqs:
+                kj = np.nonzero(ksel[ka:ke])[0] if not full else np.arange(ke - ka)
+                dk[b, ka + kj, g, :] = 0.0
+                dv[b, ka + kj, g, :] = 0.0
     for b, h, g, out in results:
         for res in out:
-            a = res["a"]
             if "dq" in res:
-                dq[b, a + res["qi"], h, :] = res["dq"]
+                dq[b, res["a"] + res["qi"], h, :] = res["dq"]
             if "dk" in res:
-                dk[b, a + res["kj"], g, :] += res["dk"]
-                dv[b, a + res["kj"], g, :] += res["dv"]
+                dk[b, res["ka"] + res["kj"], g, :] += res["dk"]
+                dv[b, res["ka"] + res["kj"], g, :] += res["dv"]
     return dq, dk, dv
 
 

@@ -64,6 +64,91 @@ def test_dense_backward_matches_finite_differences(case):
         np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-8)
 
 
+# keys outnumbering the queries and the other way round (dense rows; the masks
+# are aligned at the end of the row)
+UNEQUAL_CASES = [
+    dict(Sq=3, Sk=6, HQ=1, HKV=1, mask=dict(causal=True)),
+    dict(Sq=6, Sk=4, HQ=2, HKV=1, mask=dict(causal=True)),
+    dict(Sq=4, Sk=7, HQ=2, HKV=2, mask=dict(causal=True, window=3)),
+    dict(Sq=5, Sk=3, HQ=1, HKV=1, mask=dict(causal=False)),
+]
+
+
+@pytest.mark.parametrize("case", UNEQUAL_CASES, ids=lambda c: f"Sq{c['Sq']}Sk{c['Sk']}{c['mask']}")
+def test_unequal_lengths_backward_matches_finite_differences(case):
+    """With Sk != Sq, dQ [Sq], dK and dV [Sk] equal the central differences of
+    L = sum(O * dO), O recomputed by the forward under the end-aligned mask."""
+    rng = np.random.default_rng(17)
+    Sq, Sk, HQ, HKV, D, Dv = case["Sq"], case["Sk"], case["HQ"], case["HKV"], 3, 2
+    q, k = _rand(rng, 2, Sq, HQ, D), _rand(rng, 2, Sk, HKV, D)
+    v, do = _rand(rng, 2, Sk, HKV, Dv), _rand(rng, 2, Sq, HQ, Dv)
+    scale, mask = 0.6, case["mask"]
+    o, lse = oracle.forward(q, k, v, scale, dtype=np.float64, **mask)
+    dq, dk, dv = oracle.backward(q, k, v, o, do, lse, scale, **mask)
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    f = lambda: _loss_dense(q, k, v, do, scale, **mask)  # noqa: E731
+    for got, x in ((dq, q), (dk, k), (dv, v)):
+        np.testing.assert_allclose(got, _fd_grad(f, x), rtol=1e-6, atol=1e-8)
+
+
+@pytest.mark.parametrize("window", [-1, 3])
+def test_fewer_queries_equal_the_last_rows_of_the_square_problem(window):
+    """End alignment, checked against the square (Sq == Sk) causal evaluation:
+    Sq < Sk queries are the last Sq rows of an Sk x Sk problem whose other rows
+    carry dO = 0 (so they add nothing to dK, dV).  O, LSE, dQ of those rows and
+    all of dK, dV must agree."""
+    rng = np.random.default_rng(19)
+    Sq, Sk, D = 4, 9, 3
+    q_full, k, v = _rand(rng, 1, Sk, 2, D), _rand(rng, 1, Sk, 1, D), _rand(rng, 1, Sk, 1, D)
+    do_full = _rand(rng, 1, Sk, 2, D)
+    do_full[:, :Sk - Sq] = 0.0
+    q, do = q_full[:, Sk - Sq:], do_full[:, Sk - Sq:]
+    mask = dict(causal=True, window=window)
+    o_full, lse_full = oracle.forward(q_full, k, v, 0.5, dtype=np.float64, **mask)
+    o, lse = oracle.forward(q, k, v, 0.5, dtype=np.float64, **mask)
+    np.testing.assert_allclose(o, o_full[:, Sk - Sq:], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_full[:, :, Sk - Sq:], rtol=1e-12, atol=1e-14)
+    gq, gk, gv = oracle.backward(q_full, k, v, o_full, do_full, lse_full, 0.5, **mask)
+    dq, dk, dv = oracle.backward(q, k, v, o, do, lse, 0.5, **mask)
+    np.testing.assert_allclose(dq, gq[:, Sk - Sq:], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, gk, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, gv, rtol=1e-10, atol=1e-12)
+
+
+def test_more_queries_than_keys_leave_the_first_rows_empty():
+    """Sq > Sk under the end-aligned causal mask: the first Sq - Sk queries see
+    no key (LSE = -inf, O = 0, dQ = 0, nothing added to dK, dV) and the last Sk
+    queries behave as the square Sk x Sk causal problem."""
+    rng = np.random.default_rng(29)
+    Sq, Sk, D = 7, 4, 3
+    q, k, v, do = _rand(rng, 1, Sq, 1, D), _rand(rng, 1, Sk, 1, D), _rand(rng, 1, Sk, 1, D), _rand(rng, 1, Sq, 1, D)
+    o, lse = oracle.forward(q, k, v, 0.5, dtype=np.float64, causal=True)
+    assert np.isneginf(lse[:, :, :Sq - Sk]).all() and (o[:, :Sq - Sk] == 0).all()
+    o2, lse2 = oracle.forward(q[:, Sq - Sk:], k, v, 0.5, dtype=np.float64, causal=True)
+    np.testing.assert_allclose(o[:, Sq - Sk:], o2, rtol=1e-12, atol=1e-14)
+    dq, dk, dv = oracle.backward(q, k, v, o, do, lse, 0.5, causal=True)
+    gq, gk, gv = oracle.backward(q[:, Sq - Sk:], k, v, o2, do[:, Sq - Sk:], lse2, 0.5, causal=True)
+    assert (dq[:, :Sq - Sk] == 0).all()
+    np.testing.assert_allclose(dq[:, Sq - Sk:], gq, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, gk, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, gv, rtol=1e-10, atol=1e-12)
+
+
+def test_one_query_sees_every_key():
+    """A single query against Sk keys under the end-aligned causal mask sees all
+    of them: the same O, LSE and gradients as the unmasked evaluation."""
+    rng = np.random.default_rng(23)
+    q, k, v, do = _rand(rng, 1, 1, 2, 4), _rand(rng, 1, 6, 1, 4), _rand(rng, 1, 6, 1, 3), _rand(rng, 1, 1, 2, 3)
+    a = oracle.forward(q, k, v, 0.5, dtype=np.float64, causal=True)
+    b = oracle.forward(q, k, v, 0.5, dtype=np.float64, causal=False)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12)
+    ga = oracle.backward(q, k, v, a[0], do, a[1], 0.5, causal=True)
+    gb = oracle.backward(q, k, v, b[0], do, b[1], 0.5, causal=False)
+    for x, y in zip(ga, gb):
+        np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-14)
+
+
 def test_sparse_backward_matches_finite_differences():
     """Sparse dQ and dKV (dK plus dV on the first DV columns) against finite differences,
     with -1 padding, an out-of-range index and a repeated index in the lists."""
