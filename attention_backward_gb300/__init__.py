@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     library,
     preprocess,
     query_block_range,
+    query_block_range_qk,
     selftest_timeout,
     sparse_backward,
     sparse_land,

@@ -29,7 +29,8 @@ class Strides(ctypes.Structure):
 
 
 class Mask(ctypes.Structure):
-    _fields_ = [("causal", c_i32), ("window_left", c_i32), ("cu_seqlens", c_vp), ("num_seqs", c_i32)]
+    _fields_ = [("causal", c_i32), ("window_left", c_i32), ("cu_seqlens", c_vp), ("num_seqs", c_i32),
+                ("kv_len", c_i32)]
 
 
 _SIGS = {
@@ -58,6 +59,8 @@ _SIGS = {
     "attn_bwd_status_string": (ctypes.c_char_p, [c_i32]),
     "attn_bwd_query_block_range": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                           ctypes.POINTER(c_i32)]),
+    "attn_bwd_query_block_range_qk": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
+                                             ctypes.POINTER(c_i32)]),
     "attn_bwd_tile_schedule": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32), c_i32,
                                       ctypes.POINTER(c_i32)]),
     "attn_bwd_selftest_timeout": (c_i32, [c_vp, c_sz, c_i32, c_vp]),
@@ -126,8 +129,10 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _mask(causal: bool, window: int, cu_seqlens: Optional[torch.Tensor]) -> Mask:
-    m = Mask(1 if causal else 0, int(window), None, 0)
+def _mask(causal: bool, window: int, cu_seqlens: Optional[torch.Tensor], S: int = 0, Sk: int = 0) -> Mask:
+    """The C mask; ``kv_len`` is set when the key length Sk differs from the
+    query length S (masks then aligned at the end of each row)."""
+    m = Mask(1 if causal else 0, int(window), None, 0, int(Sk) if Sk != S else 0)
     if cu_seqlens is not None:
         _dev(cu_seqlens)
         if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
@@ -164,7 +169,7 @@ def gqa_main(q, k, v, do, dk, dv, workspace, sm_scale: float, causal: bool = Fal
     _dev(q, k, v, do, dk, dv, workspace)
     B, S, HQ, D = q.shape
     HKV = k.shape[2]
-    m = _mask(causal, window, cu_seqlens)
+    m = _mask(causal, window, cu_seqlens, S, k.shape[1])
     _status(library().attn_bwd_gqa_main(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
                                         do.data_ptr(), _bshd(do), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
                                         ctypes.byref(m), dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv),
@@ -188,7 +193,7 @@ def attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, workspace, sm_scale: float, ca
     _dev(q, k, v, o, do, lse, dq, dk, dv, workspace)
     B, S, HQ, D = q.shape
     HKV = k.shape[2]
-    m = _mask(causal, window, cu_seqlens)
+    m = _mask(causal, window, cu_seqlens, S, k.shape[1])
     _status(library().attn_bwd_gqa(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
                                    o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(),
                                    _lse_strides(lse), B, S, HQ, HKV, D, _dt(q), float(sm_scale), ctypes.byref(m),
@@ -202,7 +207,7 @@ def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, sm_scale: float, causal
     point attn_bwd."""
     _dev(q, k, v, o, do, lse, dq, dk, dv, workspace)
     B, S, H, D = q.shape
-    m = _mask(causal, window, cu_seqlens)
+    m = _mask(causal, window, cu_seqlens, S, k.shape[1])
     _status(library().attn_bwd(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
                                o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(), _lse_strides(lse),
                                B, S, H, D, _dt(q), float(sm_scale), ctypes.byref(m), dq.data_ptr(), _bshd(dq),
@@ -278,6 +283,14 @@ def query_block_range(k0: int, block_k: int, length: int, causal: bool, window: 
     return lo.value, hi.value
 
 
+def query_block_range_qk(k0: int, block_k: int, kv_len: int, q_len: int, causal: bool, window: int,
+                         block_q: int) -> tuple:
+    lo, hi = c_i32(0), c_i32(0)
+    library().attn_bwd_query_block_range_qk(k0, block_k, kv_len, q_len, int(causal), int(window), block_q,
+                                            ctypes.byref(lo), ctypes.byref(hi))
+    return lo.value, hi.value
+
+
 def tile_schedule(t: int, B: int, S: int, HKV: int, causal: bool, window: int, cu_seqlens=None) -> tuple:
     """The dense kernels' t-th tile draw: (valid, b, kv head, sequence start,
     first key, first query block, number of query blocks)."""
@@ -295,8 +308,10 @@ def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool
              cu_seqlens=None, workspace=None, stream=None):
     """dQ, dK, dV of softmax attention through the one-call entry point.
 
-    q, o, do: [B,S,HQ,D]; k, v: [B,S,HKV,D] (fp16/bf16, CUDA); lse: f32 [B,HQ,S]
-    (natural log).  Outputs are new tensors in the input dtype.
+    q, o, do: [B,S,HQ,D]; k, v: [B,Sk,HKV,D] (fp16/bf16, CUDA; Sk may differ
+    from S in a dense batch, the masks then aligned at the end of each row);
+    lse: f32 [B,HQ,S] (natural log).  Outputs are new tensors in the input
+    dtype.
     """
     _dev(q, k, v, o, do, lse)
     B, S, HQ, D = q.shape
@@ -356,7 +371,7 @@ def backward_noalloc(q, k, v, o, do, lse, sm_scale: Optional[float] = None, caus
     if sm_scale is None:
         sm_scale = D ** -0.5
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    m = _mask(causal, window, cu_seqlens)
+    m = _mask(causal, window, cu_seqlens, S, k.shape[1])
     _status(library().attn_bwd_gqa_noalloc(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v),
                                            o.data_ptr(), _bshd(o), do.data_ptr(), _bshd(do), lse.data_ptr(),
                                            _lse_strides(lse), B, S, HQ, HKV, D, _dt(q), float(sm_scale),
@@ -400,7 +415,7 @@ def backward_host(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal:
         scratch = torch.empty(need, dtype=torch.uint8, device=device)
     if streams is None:
         streams = (torch.cuda.current_stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device))
-    m = _mask(causal, window, cu_seqlens)
+    m = _mask(causal, window, cu_seqlens, S, k.shape[1])
     dq, dk, dv = out
     _status(library().attn_bwd_gqa_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                                         lse.data_ptr(), B, S, HQ, HKV, D, _dt(q), float(sm_scale), ctypes.byref(m),

@@ -200,6 +200,7 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
   for (const attn_strides_t* st : {&sq, &sk, &sv, &sdo, &sdk, &sdv})
     if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
   int causal = 0, window = -1, num_seqs = 0;
+  int64_t Sk = S;  // keys per batch row
   const int32_t* cu = nullptr;
   if (mask) {
     causal = mask->causal ? 1 : 0;
@@ -209,18 +210,21 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
     if (window == 0 || window < -1) return ATTN_ERR_INVALID_ARG;
     if (cu && (B != 1 || num_seqs < 1 || num_seqs > (1 << 20))) return ATTN_ERR_INVALID_ARG;
     if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+    if (mask->kv_len < 0 || (cu && mask->kv_len != 0 && mask->kv_len != S)) return ATTN_ERR_INVALID_ARG;
+    if (mask->kv_len > 0) Sk = mask->kv_len;
   }
+  if (B * HKV * Sk >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(B, S, HQ, D, 0);
   if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
   // key tiles per (batch, KV head): a packed batch may add one partial tile per
   // sequence.  Persistent CTAs, one per SM, draw tiles from the counter.
-  const int64_t tiles = ((S + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0)) * B * HKV;
+  const int64_t tiles = ((Sk + kDenseBM - 1) / kDenseBM + (cu ? num_seqs : 0)) * B * HKV;
   if (tiles >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   if (!encode) return ATTN_OK;  // argument checks only: no driver call
   const int BN = kDenseBN;
   DenseMaps& m = s->m;
   if (!make_map(&m.q, q, dtype, B, S, HQ, D, sq, BN) || !make_map(&m.dO, dO, dtype, B, S, HQ, D, sdo, BN) ||
-      !make_map(&m.k, k, dtype, B, S, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, S, HKV, D, sv, kDenseBM))
+      !make_map(&m.k, k, dtype, B, Sk, HKV, D, sk, kDenseBM) || !make_map(&m.v, v, dtype, B, Sk, HKV, D, sv, kDenseBM))
     return ATTN_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   // dQ partials land as [128 queries x 32 d] boxes staged with a 128-byte swizzle
@@ -228,7 +232,7 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
   DenseParams& p = s->p;
   p = DenseParams{};
   p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV);
-  p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D);
+  p.G = static_cast<int>(HQ / HKV), p.D = static_cast<int>(D), p.Sk = static_cast<int>(Sk);
   p.causal = causal, p.window = window, p.cu_seqlens = cu, p.num_seqs = num_seqs;
   p.sm_scale = sm_scale;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
@@ -418,13 +422,22 @@ void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_t len, int32_
   if (hi) *hi = h;
 }
 
+void attn_bwd_query_block_range_qk(int32_t k0, int32_t block_k, int32_t kv_len, int32_t q_len, int32_t causal,
+                                   int32_t window_left, int32_t block_q, int32_t* lo, int32_t* hi) {
+  int l = 0, h = 0;
+  if (block_k > 0 && block_q > 0 && kv_len >= 0 && q_len >= 0)
+    query_block_range_qk(k0, block_k, kv_len, q_len, kv_len - q_len, causal, window_left, block_q, &l, &h);
+  if (lo) *lo = l;
+  if (hi) *hi = h;
+}
+
 void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t causal, int32_t window_left,
                             const int32_t* cu_seqlens, int32_t num_seqs, int32_t* out) {
   if (!out) return;
   TileInfo ti{};
   if (B >= 1 && S >= 1 && HKV >= 1 && (!cu_seqlens || num_seqs >= 1)) {
     DenseParams p{};
-    p.B = B, p.S = S, p.HKV = HKV;
+    p.B = B, p.S = S, p.Sk = S, p.HKV = HKV;
     p.causal = causal ? 1 : 0, p.window = window_left;
     p.cu_seqlens = cu_seqlens, p.num_seqs = cu_seqlens ? num_seqs : 0;
     p.bn = kDenseBN;

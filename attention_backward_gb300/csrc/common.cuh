@@ -63,24 +63,34 @@ enum DeviceError : int {
 __host__ __device__ inline int imin(int a, int b) { return a < b ? a : b; }
 __host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
 
-// Query blocks [lo, hi) (blocks of ``bq`` sequence-local positions) that the
-// key tile [k0, min(k0 + bk, len)) must visit.  Key j is visible to query i
-// iff j <= i (causal or window) and i < j + W (window W > 0).
-__host__ __device__ inline void query_block_range(int k0, int bk, int len, int causal, int window, int bq, int* lo,
-                                                  int* hi) {
-  const int k1 = imin(k0 + bk, len);
-  int q_start = 0, q_end = len;
-  if (causal || window > 0) q_start = k0;
+// Query blocks [lo, hi) (blocks of ``bq`` query positions) that the key tile
+// [k0, min(k0 + bk, klen)) of a row of ``klen`` keys and ``qlen`` queries must
+// visit, query i standing at key position i + off (off = klen - qlen for a
+// dense row whose lengths differ, else 0).  Key j is visible to query i iff
+// j <= i + off (causal or window) and i + off < j + W (window W > 0).
+__host__ __device__ inline void query_block_range_qk(int k0, int bk, int klen, int qlen, int off, int causal,
+                                                     int window, int bq, int* lo, int* hi) {
+  const int k1 = imin(k0 + bk, klen);
+  int64_t q_start = 0, q_end = qlen;
+  if (causal || window > 0) q_start = static_cast<int64_t>(k0) - off;
+  if (q_start < 0) q_start = 0;
   if (window > 0) {
-    const int64_t e = static_cast<int64_t>(k1) - 1 + window;
-    q_end = e < len ? static_cast<int>(e) : len;
+    const int64_t e = static_cast<int64_t>(k1) - 1 - off + window;
+    q_end = e < qlen ? e : qlen;
   }
-  if (k0 >= len || q_start >= q_end) {
+  if (k0 >= klen || q_start >= q_end) {
     *lo = *hi = 0;
     return;
   }
-  *lo = q_start / bq;
-  *hi = (q_end + bq - 1) / bq;
+  *lo = static_cast<int>(q_start / bq);
+  *hi = static_cast<int>((q_end + bq - 1) / bq);
+}
+
+// The same for equal query and key lengths (the sequence-local positions of a
+// packed sequence or of a dense row with Sk == Sq).
+__host__ __device__ inline void query_block_range(int k0, int bk, int len, int causal, int window, int bq, int* lo,
+                                                  int* hi) {
+  query_block_range_qk(k0, bk, len, len, 0, causal, window, bq, lo, hi);
 }
 
 // Sequence bounds of batch row b / packed sequence n, clamped to [0, S].

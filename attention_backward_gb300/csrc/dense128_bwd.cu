@@ -78,7 +78,7 @@ constexpr int OFF_DS = OFF_STAGE + ST * STAGE;
 constexpr int OFF_LSE = OFF_DS + 2 * DS_BLOCK;
 constexpr int OFF_DELTA = OFF_LSE + ST * BN * 4;
 constexpr int OFF_RING = OFF_DELTA + ST * BN * 4;
-constexpr int OFF_BAR = OFF_RING + 64;
+constexpr int OFF_BAR = OFF_RING + 2 * static_cast<int>(sizeof(TileInfo));
 constexpr int NBAR = 32;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM = OFF_MISC + 64;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       if (!ti.valid) break;
       if (tc >= 1 && !(ok = mbar_wait_warp(&bars[KV_FREE], (tc - 1) & 1, wc, kErrWaitKVFree))) break;
       int kr0, kr1;
-      tail_rows(ti.seq_start + ti.k0, BM, tail0, p.S, &kr0, &kr1);
+      tail_rows(ti.seq_start + ti.k0, BM, p.cu_seqlens ? tail0 : p.Sk, p.Sk, &kr0, &kr1);
       if (kr0 < kr1) {
         static_assert(KV_TILE == Q_TILE, "one tail load size");
         if (!(ok = load_zeroed(sm + OFF_K, &maps.k, sm + OFF_V, &maps.v, ti.g, ti.seq_start + ti.k0, ti.b, kr0, kr1,
@@ -333,8 +333,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
           const int q = qq + lane + 32 * i;
-          nl[i] = q < ti.len ? p.lse2[rb + q] : 0.f;
-          nd[i] = q < ti.len ? p.delta[rb + q] : 0.f;
+          nl[i] = q < ti.qlen ? p.lse2[rb + q] : 0.f;
+          nd[i] = q < ti.qlen ? p.delta[rb + q] : 0.f;
         }
       };
       if (n > 0) load_rows(0);
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
             }
           }
           const int64_t rf = (static_cast<int64_t>(ti.b) * p.HQ + hf) * p.S + ti.seq_start + qf;
-          if (lane < BN / 32 && qf + lane * 32 < ti.len) {
+          if (lane < BN / 32 && qf + lane * 32 < ti.qlen) {
             prefetch_l2(p.lse2 + rf + lane * 32);
             prefetch_l2(p.delta + rf + lane * 32);
           }
@@ -529,8 +529,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         const int q0 = (ti.qlo + j % ti.nq) * BN;
         const int qc0 = q0 + wg * HALF;  // first (sequence-local) query of my columns
         // fully visible block: every key and query in range and inside the mask
-        const bool full_vis = ti.k0 + BM <= ti.len && q0 + BN <= ti.len && (!cm || q0 >= ti.k0 + BM - 1) &&
-                              (W <= 0 || q0 + BN - 1 < ti.k0 + W);
+        const bool full_vis = ti.k0 + BM <= ti.len && q0 + BN <= ti.qlen &&
+                              (!cm || q0 + ti.off >= ti.k0 + BM - 1) && (W <= 0 || q0 + BN - 1 + ti.off < ti.k0 + W);
         const float4* lse4 = reinterpret_cast<const float4*>(s_lse + st * BN + wg * HALF);
         const float4* dlt4 = reinterpret_cast<const float4*>(s_delta + st * BN + wg * HALF);
         if (!(ok = mbar_wait_warp(&bars[FULL0 + st], (gs / ST) & 1, wc, kErrWaitStageFull))) break;
@@ -559,9 +559,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int cc = 4 * c4 + e, q = qc0 + cc;
-              bool vis = kvalid && q < ti.len;
-              if (cm) vis = vis && kpos <= q;
-              if (W > 0) vis = vis && q < kpos + W;
+              bool vis = kvalid && q < ti.qlen;
+              if (cm) vis = vis && kpos <= q + ti.off;
+              if (W > 0) vis = vis && q + ti.off < kpos + W;
               pv[cc] = vis ? ex2(fmaf(__uint_as_float(sr[cc]), p.scale_log2, -l4[e])) : 0.f;
             }
           }

@@ -6,8 +6,11 @@
 
 namespace ab {
 
+// len: keys of the tile's sequence; qlen: its queries; off: the key position
+// of query 0 (qlen, off differ from len, 0 only in a dense row with Sk != S).
 struct TileInfo {
   int b, g, seq_start, len, k0, qlo, nq, valid;
+  int qlen, off;
 };
 
 // TMEM column, relative to a step's S^T buffer, of the 16-bit pair of P^T
@@ -39,7 +42,7 @@ static __host__ __device__ __forceinline__ TileInfo decode_tile(int t, const Den
   if (t < 0) return ti;
   int bh, r;
   if (p.cu_seqlens == nullptr) {
-    const int nt = (p.S + kDenseBM - 1) / kDenseBM;  // key tiles per pair
+    const int nt = (p.Sk + kDenseBM - 1) / kDenseBM;  // key tiles per pair
     const int grp = imin(BH, kTileGroup);
     const int gi = t / (grp * nt);
     const int g0 = gi * grp;
@@ -62,7 +65,8 @@ static __host__ __device__ __forceinline__ TileInfo decode_tile(int t, const Den
       const int nt = e > a ? (e - a + kDenseBM - 1) / kDenseBM : 0;
       if (r < nt) {
         ti.seq_start = a;
-        ti.len = e - a;
+        ti.len = ti.qlen = e - a;
+        ti.off = 0;
         found = true;
         break;
       }
@@ -71,11 +75,13 @@ static __host__ __device__ __forceinline__ TileInfo decode_tile(int t, const Den
     if (!found) return ti;
   } else {
     ti.seq_start = 0;
-    ti.len = p.S;
+    ti.len = p.Sk;
+    ti.qlen = p.S;
+    ti.off = p.Sk - p.S;
   }
   ti.k0 = r * kDenseBM;
   int lo, hi;
-  query_block_range(ti.k0, kDenseBM, ti.len, p.causal, p.window, p.bn, &lo, &hi);
+  query_block_range_qk(ti.k0, kDenseBM, ti.len, ti.qlen, ti.off, p.causal, p.window, p.bn, &lo, &hi);
   ti.qlo = lo;
   ti.nq = hi - lo;
   ti.valid = 1;

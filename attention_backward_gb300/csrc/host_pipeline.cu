@@ -78,8 +78,10 @@ extern "C" attn_status_t attn_bwd_gqa_host(const void* q, const void* k, const v
   if (dtype != ATTN_DT_F16 && dtype != ATTN_DT_BF16) return ATTN_ERR_UNSUPPORTED;
   if (HQ / HKV > (dtype == ATTN_DT_BF16 ? ATTN_BWD_MAX_GROUP_BF16 : ATTN_BWD_MAX_GROUP_F16)) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
+  // chunks copy K/V as [B,S,HKV,D]: key rows of another length are not served here
   if (mask && (mask->window_left == 0 || mask->window_left < -1 ||
-               (mask->cu_seqlens && (B != 1 || mask->num_seqs < 1 || mask->num_seqs > (1 << 20)))))
+               (mask->cu_seqlens && (B != 1 || mask->num_seqs < 1 || mask->num_seqs > (1 << 20))) ||
+               (mask->kv_len != 0 && mask->kv_len != S)))
     return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
   const HostLayout L = host_layout(B, S, HQ, HKV, D, chunks);

@@ -38,6 +38,7 @@ struct LandParams {
 
 struct DenseParams {
   int B, S, HQ, HKV, G, D;
+  int Sk;  // key/value rows per batch row (S unless a dense row has more or fewer keys than queries)
   int causal, window;
   const int* cu_seqlens;
   int num_seqs;

@@ -83,10 +83,17 @@ typedef struct {
 /* Which keys a query sees, within one sequence.  Sequences: each batch row,
  * or, when cu_seqlens is given (B must be 1), the packed ranges
  * [cu_seqlens[n], cu_seqlens[n+1]) along S.  Positions are local to a
- * sequence.  Query i sees key j iff
+ * sequence.  Query i stands at key position i + off, where off = Sk - S for
+ * a dense row of S queries and Sk keys and off = 0 otherwise (the masks are
+ * aligned at the end of the row, so the last query sees the last key; the
+ * pages define the masks for square problems only, and this is the reading
+ * taken for rows whose lengths differ).  Query i sees key j iff
  *   causal == 0 and window_left < 0 : always,
- *   causal != 0                     : j <= i  (the page's "cols <= rows"),
- *   window_left = W > 0             : i - W < j <= i  (implies causal).
+ *   causal != 0                     : j <= i + off  (the page's "cols <= rows"),
+ *   window_left = W > 0             : i + off - W < j <= i + off  (implies causal).
+ * A query that sees no key (i + off < 0) gets dQ = 0 and adds nothing to dK,
+ * dV; its LSE row is expected to be -inf (any value is accepted: it is never
+ * used as an operand).
  * cu_seqlens: device int32 [num_seqs + 1], non-decreasing from 0 and ending
  * at most at S (the kernels clamp to S); NULL for dense batches.  Rows past
  * cu_seqlens[num_seqs] belong to no sequence: the kernels never use their Q,
@@ -94,12 +101,15 @@ typedef struct {
  * in shared memory after the load), so they may hold anything, NaN included;
  * dQ rows there are written as zero and dK/dV rows there are not written.
  * No longest-sequence length is needed: the persistent kernels compute the
- * tile count of every sequence on the device. */
+ * tile count of every sequence on the device.
+ * kv_len: keys per batch row of a dense batch, Sk (k, v, dk, dv are then
+ * [B,Sk,HKV,D]); 0 means Sk = S.  Must be 0 or S when cu_seqlens is given. */
 typedef struct {
   int32_t causal;
   int32_t window_left;
   const int32_t* cu_seqlens;
   int32_t num_seqs;
+  int32_t kv_len;
 } attn_mask_t;
 
 /* Bytes of workspace one backward call needs: a 256-byte header (device error
@@ -134,7 +144,8 @@ ATTN_BWD_API attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so,
  * TileOPs page's three launches behind one op call ("Summary": preprocess,
  * main kernel, dQ landing), queued on ``stream`` after every argument has
  * been checked, so a call either queues all three or nothing.
- *   q, o, dO, dq : [B,S,HQ,D] 16-bit;  k, v, dk, dv : [B,S,HKV,D] 16-bit;
+ *   q, o, dO, dq : [B,S,HQ,D] 16-bit;  k, v, dk, dv : [B,Sk,HKV,D] 16-bit
+ *   (Sk = mask->kv_len if mask and kv_len > 0, else S);
  *   lse : f32 natural-log LSE [B,HQ,S] of the forward with strides slse
  *   (b, s, h);  dq, dk, dv are written (dK and dV once per key row by their
  *   owning CTA, dQ = sm_scale * the f32 sum of its partials).
@@ -251,6 +262,14 @@ ATTN_BWD_API const char* attn_bwd_status_string(attn_status_t status);
 ATTN_BWD_API void attn_bwd_query_block_range(int32_t k0, int32_t block_k, int32_t len, int32_t causal, int32_t window_left,
                                 int32_t block_q, int32_t* lo, int32_t* hi);
 
+/* The same for a dense row of ``q_len`` queries and ``kv_len`` keys whose
+ * masks are aligned at the end of the row (query i at key position
+ * i + kv_len - q_len, as attn_mask_t describes); with q_len == kv_len it
+ * equals attn_bwd_query_block_range. */
+ATTN_BWD_API void attn_bwd_query_block_range_qk(int32_t k0, int32_t block_k, int32_t kv_len, int32_t q_len,
+                                                int32_t causal, int32_t window_left, int32_t block_q, int32_t* lo,
+                                                int32_t* hi);
+
 /* Host-side schedule helper, exported so that the persistent tile order of the
  * dense kernels can be checked on the host.  Tile ``t`` is the t-th draw from
  * the tile counter of a launch over B batch rows, S positions and HKV KV heads
@@ -336,7 +355,8 @@ ATTN_BWD_API size_t attn_bwd_host_scratch_size(int64_t B, int64_t S, int64_t HQ,
  *   [B,S,HKV,D] 16-bit, contiguous;  lse : host f32 [B,HQ,S] (natural log),
  *   contiguous.  Host buffers should be page-locked (with pageable memory the
  *   copies are correct but do not overlap); dq, dk, dv are written.
- *   mask : as for attn_bwd_gqa (cu_seqlens in device memory).
+ *   mask : as for attn_bwd_gqa (cu_seqlens in device memory); kv_len must be
+ *   0 or S here (ATTN_ERR_INVALID_ARG otherwise).
  *   scratch : device memory of attn_bwd_host_scratch_size(...) bytes, 256-byte
  *   aligned, owned by the caller; it starts with the workspace of one chunk,
  *   so attn_bwd_check_error(scratch, stream, ...) reports device errors.

@@ -70,6 +70,26 @@ def test_query_block_range_matches_brute_force(ab, cu, causal, window, bq):
             assert set(range(lo, hi)) == set((rows // bq).tolist()), (a, e, k0, lo, hi)
 
 
+@pytest.mark.parametrize("sq,sk", [(100, 300), (300, 100), (257, 1000), (1000, 257), (128, 129), (129, 128),
+                                   (1, 700), (700, 1)])
+@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (True, 1), (True, 100)])
+@pytest.mark.parametrize("bq", [64, 128])
+def test_query_block_range_of_unequal_rows_matches_brute_force(ab, sq, sk, causal, window, bq):
+    """A dense row of sq queries and sk keys, masks aligned at the end of the
+    row (the oracle's visibility with off = sk - sq): every query block with a
+    visible pair is visited and no other block is."""
+    from oracle.attention import _visible_block
+
+    vis = _visible_block(np.arange(sq), np.arange(sk), causal, window, sk - sq)
+    for k0 in range(0, sk, 128):
+        lo, hi = ab.query_block_range_qk(k0, 128, sk, sq, causal, window, bq)
+        rows = np.nonzero(vis[:, k0:k0 + 128].any(axis=1))[0]
+        assert set(range(lo, hi)) == set((rows // bq).tolist()), (k0, lo, hi)
+    for k0 in range(0, 1000, 128):  # equal lengths: the square helper
+        assert ab.query_block_range_qk(k0, 128, 1000, 1000, causal, window, bq) == \
+            ab.query_block_range(k0, 128, 1000, causal, window, bq)
+
+
 def test_causal_step_count_matches_the_page(ab):
     """The causal kernel visits 272 of the 512 (key block, query block) steps of
     a 2048-row head at 128/64 blocks (TileOPs page, analysis bullets)."""
@@ -204,6 +224,8 @@ BAD_CALLS = [
     ("window -2", dict(mask="w-2"), 1),
     ("varlen B > 1", dict(mask="varlen"), 1),
     ("varlen no sequences", dict(mask="varlen0", B=1), 1),
+    ("negative kv_len", dict(mask="kvneg"), 1),
+    ("kv_len with varlen", dict(mask="kvvarlen", B=1), 1),
     ("NaN scale", dict(scale=float("nan")), 1),
     ("infinite scale", dict(scale=float("inf")), 1),
     ("head dim 96", dict(D=96), 2),
@@ -220,7 +242,8 @@ def _resolve(ab, kw):
         kw["sq"] = S(2048 * 32 * 128, 32 * 128 + 4, 128)  # 8-byte head stride: not a 16-byte multiple
     if "mask" in kw:
         kw["mask"] = {None: M(1, 0, None, 0), "w-2": M(1, -2, None, 0), "varlen": M(1, -1, 1 << 20, 3),
-                      "varlen0": M(1, -1, 1 << 20, 0)}[kw["mask"]]
+                      "varlen0": M(1, -1, 1 << 20, 0), "kvneg": M(1, -1, None, 0, -5),
+                      "kvvarlen": M(1, -1, 1 << 20, 3, 100)}[kw["mask"]]
     return kw
 
 
@@ -312,11 +335,12 @@ def test_landing_and_noalloc_limits_return_before_any_launch(ab):
     assert noalloc() == 3
     assert noalloc(D=96) == 2
     # host-buffer entry point: null scratch, unsupported head dim, misaligned scratch
-    def host(scratch=fake, D=128, chunks=4):
+    def host(scratch=fake, D=128, chunks=4, mask=m):
         return lib.attn_bwd_gqa_host(fake, fake, fake, fake, fake, fake, 2, 2048, 32, 32, D, 0, 0.1,
-                                     ctypes.byref(m), fake, fake, fake, scratch, 1 << 40, chunks, None, None, None)
+                                     ctypes.byref(mask), fake, fake, fake, scratch, 1 << 40, chunks, None, None, None)
 
     assert host(scratch=None) == 1
     assert host(D=96) == 2
     assert host(scratch=fake + 16) == 1
+    assert host(mask=ab._binding.Mask(1, -1, None, 0, 4096)) == 1   # key rows of another length
     assert lib.attn_bwd_host_scratch_size(2, 2048, 32, 32, 96, 4) == 0

@@ -68,6 +68,47 @@ def test_small_cases_match_oracle(w):
     assert_close(dv, rv, w, "dv")
 
 
+# Dense rows whose key length differs from the query length (kv_len in the C
+# mask): the masks are aligned at the end of the row, query i at key position
+# i + Sk - S.  Cases cover more and fewer keys than queries under every mask
+# kind and both head dims, key tiles that no query sees (dK = dV = 0 written),
+# queries that see no key (dQ = 0, LSE -inf from the forward), one query, one
+# key, and ragged tiles on both sides.
+UNEQUAL = [
+    inputs.scaled(C1, name="sk520_sq200_causal_b2_f16", B=2, S=200, Sk=520),
+    inputs.scaled(C1, name="sq520_sk200_causal_f16", S=520, Sk=200),
+    inputs.scaled(C3, name="sk390_sq130_noncausal_g4_bf16", S=130, Sk=390, HQ=8, HKV=2),
+    inputs.scaled(C3, name="sq300_sk170_causal_g2_bf16", S=300, Sk=170, HQ=4, HKV=2, causal=True),
+    inputs.scaled(C4, name="sk700_sq300_w100_d64", S=300, Sk=700, HQ=4, HKV=2, window=100, cu_seqlens=None),
+    inputs.scaled(C4, name="sq700_sk300_w64_d64_f16", S=700, Sk=300, HQ=2, HKV=1, window=64, cu_seqlens=None,
+                  dtype="f16"),
+    inputs.scaled(C4, name="sq390_sk130_noncausal_d64_b2", B=2, S=390, Sk=130, HQ=2, HKV=2, causal=False, window=-1,
+                  cu_seqlens=None),
+    inputs.scaled(C4, name="sk300_sq129_causal_d64_g4", S=129, Sk=300, HQ=8, HKV=2, window=-1, cu_seqlens=None),
+    inputs.scaled(C1, name="sq1_sk700_causal", S=1, Sk=700),
+    inputs.scaled(C1, name="sq1_sk700_noncausal", S=1, Sk=700, causal=False),
+    inputs.scaled(C4, name="sq300_sk1_causal_d64", S=300, Sk=1, HQ=2, HKV=1, window=-1, cu_seqlens=None),
+]
+
+
+@pytest.mark.parametrize("w", UNEQUAL, ids=lambda w: w.name)
+def test_unequal_query_and_key_lengths_match_oracle(w):
+    prob = dense_problem(w)
+    q, k, v, o, do, lse = prob
+    assert k.shape[1] == w.Sk != w.S
+    rq, rk, rv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, **mask_of(w))
+    dq, dk, dv, _ = run_dense(w, prob)
+    assert tuple(dk.shape) == k.shape and tuple(dv.shape) == v.shape
+    assert_close(dq, rq, w, "dq")
+    assert_close(dk, rk, w, "dk")
+    assert_close(dv, rv, w, "dv")
+    if w.S > w.Sk and w.causal:  # the first S - Sk queries see no key
+        assert (to_np(dq)[:, : w.S - w.Sk] == 0).all()
+    # the split launches take the key length from the same mask field
+    b = run_dense(w, prob, split=True)
+    assert (to_np(b[1]) == to_np(dk)).all() and (to_np(b[2]) == to_np(dv)).all()
+
+
 def test_split_launches_match_one_call():
     """The three launches called one by one (attn_bwd_preprocess,
     attn_bwd_gqa_main, attn_bwd_dq_land) give the one-call results: the same
