@@ -27,7 +27,7 @@
 // issued before dV/dK/dQ of step i, so the softmax of one step overlaps the
 // tensor work of the previous one.  P^T and dS^T of a step are written over
 // that step's S^T columns, and its dQ goes there once dK has read them.
-// Q/dO come through a 3-stage TMA ring; the f32 dQ partial of a step is
+// Q/dO come through a 4-stage TMA ring; the f32 dQ partial of a step is
 // staged in the step's own stage and the stage goes back to the producer once
 // the dQ reduces have read it.  No stage or accumulator is reused before an
 // mbarrier shows that its last reader is done (the two pipelining faults the

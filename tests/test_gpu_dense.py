@@ -109,6 +109,26 @@ def test_unequal_query_and_key_lengths_match_oracle(w):
     assert (to_np(b[1]) == to_np(dk)).all() and (to_np(b[2]) == to_np(dv)).all()
 
 
+# Every group size the ABI accepts, one small causal case each: G = 1..16 in
+# fp16, G = 1..8 in bf16, alternating head dims 64 and 128, two KV heads.
+EVERY_G = [
+    inputs.scaled(C3, name=f"every_g{g}_{dt}_d{d}", S=200, HQ=2 * g, HKV=2, D=d, Dv=d, causal=True, dtype=dt,
+                  seed=20260100 + g)
+    for dt, gmax in (("f16", 16), ("bf16", 8)) for g in range(1, gmax + 1) for d in ((64, 128)[g % 2],)
+]
+
+
+@pytest.mark.parametrize("w", EVERY_G, ids=lambda w: w.name)
+def test_every_accepted_group_size_matches_oracle(w):
+    prob = dense_problem(w)
+    q, k, v, o, do, lse = prob
+    rq, rk, rv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, **mask_of(w))
+    dq, dk, dv, _ = run_dense(w, prob)
+    assert_close(dq, rq, w, "dq")
+    assert_close(dk, rk, w, "dk")
+    assert_close(dv, rv, w, "dv")
+
+
 def test_split_launches_match_one_call():
     """The three launches called one by one (attn_bwd_preprocess,
     attn_bwd_gqa_main, attn_bwd_dq_land) give the one-call results: the same
