@@ -11,10 +11,12 @@ from ._binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_gqa,
     attn_bwd_sparse,
+    attn_fwd_gqa,
     backward,
     backward_host,
     check_error,
     dq_land,
+    forward,
     gqa_main,
     host_scratch_size,
     library,

@@ -59,6 +59,8 @@ _SIGS = {
     "attn_bwd_status_string": (ctypes.c_char_p, [c_i32]),
     "attn_bwd_query_block_range": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                           ctypes.POINTER(c_i32)]),
+    "attn_fwd_gqa": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64, c_i32,
+                             c_f32, ctypes.POINTER(Mask), c_vp, Strides, c_vp, Strides, c_vp, c_sz, c_vp]),
     "attn_bwd_query_block_range_qk": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                              ctypes.POINTER(c_i32)]),
     "attn_bwd_tile_schedule": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32), c_i32,
@@ -213,6 +215,35 @@ def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, sm_scale: float, causal
                                B, S, H, D, _dt(q), float(sm_scale), ctypes.byref(m), dq.data_ptr(), _bshd(dq),
                                dk.data_ptr(), _bshd(dk), dv.data_ptr(), _bshd(dv), workspace.data_ptr(),
                                workspace.numel(), _stream(stream)), "attn_bwd")
+
+
+def attn_fwd_gqa(q, k, v, o, lse, workspace, sm_scale: float, causal: bool = False, window: int = -1,
+                 cu_seqlens=None, stream=None) -> None:
+    """The forward into caller-owned o (16-bit [B,S,HQ,D]) and lse (f32
+    [B,HQ,S]) (see attn_fwd_gqa)."""
+    _dev(q, k, v, o, lse, workspace)
+    B, S, HQ, D = q.shape
+    HKV = k.shape[2]
+    m = _mask(causal, window, cu_seqlens, S, k.shape[1])
+    _status(library().attn_fwd_gqa(q.data_ptr(), _bshd(q), k.data_ptr(), _bshd(k), v.data_ptr(), _bshd(v), B, S,
+                                   HQ, HKV, D, _dt(q), float(sm_scale), ctypes.byref(m), o.data_ptr(), _bshd(o),
+                                   lse.data_ptr(), _lse_strides(lse), workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream)), "attn_fwd_gqa")
+
+
+def forward(q, k, v, sm_scale: Optional[float] = None, causal: bool = False, window: int = -1, cu_seqlens=None,
+            workspace=None, stream=None):
+    """O and the natural-log LSE [B,HQ,S] of softmax attention (new tensors)."""
+    _dev(q, k, v)
+    B, S, HQ, D = q.shape
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, HQ, S, dtype=torch.float32, device=q.device)
+    attn_fwd_gqa(q, k, v, o, lse, workspace, sm_scale, causal, window, cu_seqlens, stream)
+    return o, lse
 
 
 def _idx_strides(idx) -> Strides:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn_bwd.so")
-SOURCES = ["api.cu", "preprocess.cu", "dense_bwd.cu", "dense128_bwd.cu", "sparse_bwd.cu", "noalloc.cu", "host_pipeline.cu"]
+SOURCES = ["api.cu", "preprocess.cu", "dense_bwd.cu", "dense128_bwd.cu", "dense_fwd.cu", "sparse_bwd.cu", "noalloc.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-I", CSRC]

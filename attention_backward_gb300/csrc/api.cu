@@ -173,6 +173,31 @@ attn_status_t run_preprocess(const PreSetup& s, void* stream) {
   return launch_status(launch_preprocess(s.p, s.bf16, sm_count() * 8, static_cast<cudaStream_t>(stream)));
 }
 
+// The mask of a dense call: causal, window, packed sequences and the key
+// length (0 in kv_len: the query length S).
+struct MaskArgs {
+  int causal = 0, window = -1, num_seqs = 0;
+  const int32_t* cu = nullptr;
+  int64_t Sk = 0;
+};
+
+attn_status_t parse_mask(const attn_mask_t* mask, int64_t B, int64_t S, MaskArgs* m) {
+  *m = MaskArgs{};
+  m->Sk = S;
+  if (!mask) return ATTN_OK;
+  m->causal = mask->causal ? 1 : 0;
+  m->window = mask->window_left;
+  m->cu = mask->cu_seqlens;
+  m->num_seqs = mask->num_seqs;
+  if (m->window == 0 || m->window < -1) return ATTN_ERR_INVALID_ARG;
+  if (m->cu && (B != 1 || m->num_seqs < 1 || m->num_seqs > (1 << 20))) return ATTN_ERR_INVALID_ARG;
+  if (m->cu && (reinterpret_cast<uintptr_t>(m->cu) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  if (mask->kv_len < 0 || (m->cu && mask->kv_len != 0 && mask->kv_len != S)) return ATTN_ERR_INVALID_ARG;
+  if (mask->kv_len > 0) m->Sk = mask->kv_len;
+  if (!m->cu) m->num_seqs = 0;
+  return ATTN_OK;
+}
+
 struct DenseSetup {
   DenseParams p;
   DenseMaps m;
@@ -199,20 +224,11 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
     if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
   for (const attn_strides_t* st : {&sq, &sk, &sv, &sdo, &sdk, &sdv})
     if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
-  int causal = 0, window = -1, num_seqs = 0;
-  int64_t Sk = S;  // keys per batch row
-  const int32_t* cu = nullptr;
-  if (mask) {
-    causal = mask->causal ? 1 : 0;
-    window = mask->window_left;
-    cu = mask->cu_seqlens;
-    num_seqs = mask->num_seqs;
-    if (window == 0 || window < -1) return ATTN_ERR_INVALID_ARG;
-    if (cu && (B != 1 || num_seqs < 1 || num_seqs > (1 << 20))) return ATTN_ERR_INVALID_ARG;
-    if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
-    if (mask->kv_len < 0 || (cu && mask->kv_len != 0 && mask->kv_len != S)) return ATTN_ERR_INVALID_ARG;
-    if (mask->kv_len > 0) Sk = mask->kv_len;
-  }
+  MaskArgs ma;
+  if (const attn_status_t mst = parse_mask(mask, B, S, &ma); mst != ATTN_OK) return mst;
+  const int causal = ma.causal, window = ma.window, num_seqs = ma.num_seqs;
+  const int32_t* cu = ma.cu;
+  const int64_t Sk = ma.Sk;  // keys per batch row
   if (B * HKV * Sk >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(B, S, HQ, D, 0);
   if (workspace_bytes < static_cast<size_t>(L.total)) return ATTN_ERR_WORKSPACE;
@@ -252,6 +268,67 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
 
 attn_status_t run_dense(const DenseSetup& s, void* stream) {
   return launch_status(launch_dense(s.p, s.m, s.bf16, s.grid, static_cast<cudaStream_t>(stream)));
+}
+
+struct FwdSetup {
+  FwdParams p;
+  FwdMaps m;
+  bool bf16;
+  int grid;
+  void* workspace;
+};
+
+attn_status_t setup_fwd(FwdSetup* s, const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
+                        const void* v, attn_strides_t sv, int64_t B, int64_t S, int64_t HQ, int64_t HKV, int64_t D,
+                        attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* o, attn_strides_t so,
+                        float* lse, attn_strides_t slse, void* workspace, size_t workspace_bytes) {
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || HQ < 1 || HKV < 1 || HQ % HKV != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!dtype_ok(dtype)) return ATTN_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  for (const attn_strides_t* st : {&sq, &sk, &sv, &so})
+    if (!strides_ok(*st)) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || slse.b < 0 || slse.s < 0 || slse.h < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < static_cast<size_t>(kHeaderBytes)) return ATTN_ERR_WORKSPACE;
+  MaskArgs ma;
+  if (const attn_status_t mst = parse_mask(mask, B, S, &ma); mst != ATTN_OK) return mst;
+  if (S >= (int64_t(1) << 31) || B * HQ * S >= (int64_t(1) << 31) || B * HKV * ma.Sk >= (int64_t(1) << 31) ||
+      B > 65535 || HQ > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  // units of two 128-row query tiles per (batch row or sequence, query head); a
+  // packed batch may add one partial unit per sequence
+  const int64_t units = ((S + 255) / 256 + (ma.cu ? ma.num_seqs : 0)) * B * HQ;
+  if (units >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+  FwdMaps& m = s->m;
+  if (!make_map(&m.q, q, dtype, B, S, HQ, D, sq, 128) || !make_map(&m.k, k, dtype, B, ma.Sk, HKV, D, sk, 128) ||
+      !make_map(&m.v, v, dtype, B, ma.Sk, HKV, D, sv, 128))
+    return ATTN_ERR_INVALID_ARG;
+  FwdParams& p = s->p;
+  p = FwdParams{};
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.Sk = static_cast<int>(ma.Sk);
+  p.HQ = static_cast<int>(HQ), p.HKV = static_cast<int>(HKV), p.G = static_cast<int>(HQ / HKV);
+  p.D = static_cast<int>(D);
+  p.causal = ma.causal, p.window = ma.window, p.cu_seqlens = ma.cu, p.num_seqs = ma.num_seqs;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.o = static_cast<uint8_t*>(o), p.so_b = so.b, p.so_s = so.s, p.so_h = so.h;
+  p.lse = lse, p.sl_b = slse.b, p.sl_s = slse.s, p.sl_h = slse.h;
+  p.err = &static_cast<WsHeader*>(workspace)->err;
+  p.timeout_ns = wait_limit_ns();
+  s->bf16 = dtype == ATTN_DT_BF16;
+  s->grid = static_cast<int>(units);
+  s->workspace = workspace;
+  return ATTN_OK;
+}
+
+attn_status_t run_fwd(const FwdSetup& s, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the error word starts clear; the kernel records the first wait that ran out
+  if (cudaMemsetAsync(s.workspace, 0, kHeaderBytes, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return launch_status(launch_fwd(s.p, s.m, s.bf16, s.grid, st));
 }
 
 struct LandSetup {
@@ -496,6 +573,16 @@ attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn
   if ((st = run_preprocess(pre, stream)) != ATTN_OK) return st;
   if ((st = run_dense(main, stream)) != ATTN_OK) return st;
   return run_land(land, stream);
+}
+
+attn_status_t attn_fwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,
+                           attn_strides_t sv, int64_t B, int64_t S, int64_t HQ, int64_t HKV, int64_t D,
+                           attn_dtype_t dtype, float sm_scale, const attn_mask_t* mask, void* o, attn_strides_t so,
+                           float* lse, attn_strides_t slse, void* workspace, size_t workspace_bytes, void* stream) {
+  FwdSetup f;
+  const attn_status_t st = setup_fwd(&f, q, sq, k, sk, v, sv, B, S, HQ, HKV, D, dtype, sm_scale, mask, o, so, lse,
+                                     slse, workspace, workspace_bytes);
+  return st != ATTN_OK ? st : run_fwd(f, stream);
 }
 
 attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,

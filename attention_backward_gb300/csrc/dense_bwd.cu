@@ -567,16 +567,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
               pv[4 * c4 + e] = ex2(fmaf(__uint_as_float(sr[4 * c4 + e]), p.scale_log2, -l4[e]));
           }
         } else {
+          // my columns cc in [c_lo, c_hi) are visible: a real query (cc < qlen -
+          // qc0), at or after my key (kpos <= qc0 + cc + off) and within the window
+          // (qc0 + cc + off < kpos + W); one range per step, two compares a column
+          const int64_t d0 = static_cast<int64_t>(kpos) - qc0 - ti.off;
+          const int64_t hi = W > 0 ? d0 + W : HALF;
+          const int c_lo = cm ? static_cast<int>(d0 < 0 ? 0 : (d0 > HALF ? HALF : d0)) : 0;
+          const int c_hi = imin(ti.qlen - qc0, static_cast<int>(hi < 0 ? 0 : (hi > HALF ? HALF : hi)));
 #pragma unroll
           for (int c4 = 0; c4 < HALF / 4; ++c4) {
             const float4 t = lse4[c4];
             const float l4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int cc = 4 * c4 + e, q = qc0 + cc;
-              bool vis = kvalid && q < ti.qlen;
-              if (cm) vis = vis && kpos <= q + ti.off;
-              if (W > 0) vis = vis && q + ti.off < kpos + W;
+              const int cc = 4 * c4 + e;
+              const bool vis = kvalid && cc >= c_lo && cc < c_hi;
               pv[cc] = vis ? ex2(fmaf(__uint_as_float(sr[cc]), p.scale_log2, -l4[e])) : 0.f;
             }
           }

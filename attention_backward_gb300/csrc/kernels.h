@@ -62,6 +62,27 @@ struct DenseMaps {
   CUtensorMap dq;  // f32 dQ accumulator [B,S,HQ,D] (bulk reduce-add target)
 };
 
+// The dense forward (dense_fwd.cu): O and the natural-log LSE.
+struct FwdParams {
+  int B, S, Sk, HQ, HKV, G, D;
+  int causal, window;
+  const int* cu_seqlens;
+  int num_seqs;
+  float scale_log2;  // sm_scale * log2(e), > 0
+  uint8_t* o;        // 16-bit [B,S,HQ,D]
+  int64_t so_b, so_s, so_h;
+  float* lse;  // f32, lse[b*sl_b + h*sl_h + s*sl_s]
+  int64_t sl_b, sl_s, sl_h;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+struct FwdMaps {
+  CUtensorMap q, k, v;  // box 64 d x 128 rows of one head
+};
+
+cudaError_t launch_fwd(const FwdParams& p, const FwdMaps& m, bool bf16, int grid, cudaStream_t st);
+
 struct SparseParams {
   int B, S, SKV, H, HKV, topk;
   int gh;            // query heads per KV group (at most 64; a unit pads them to 64)

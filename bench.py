@@ -190,39 +190,44 @@ def traffic_record(kernel_src: str, name: str):
 # ------------------------------------------------------------------ inputs (GPU arm)
 
 def gpu_dense_inputs(w, device):
-    """Q, K, V, dO from the seeded generator; O and LSE from a float32 torch
-    forward on the device (input preparation only; it is not timed)."""
+    """Q, K, V, dO from the seeded generator; O and LSE from the library's own
+    forward (attn_fwd_gqa) on the device (input preparation; it is timed
+    separately, not as part of the backward's step)."""
     import torch
 
+    import attention_backward_gb300 as ab
     from attention_backward_gb300 import inputs
 
     q, k, v, do = inputs.dense_inputs(w)
     tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     tq, tk, tv, tdo = (torch.from_numpy(a).to(device).to(tdt) for a in (q, k, v, do))
-    G = w.HQ // w.HKV
-    o = torch.empty_like(tdo)
-    lse = torch.empty(w.B, w.HQ, w.S, dtype=torch.float32, device=device)
-    seqs = [(0, w.S)] if w.cu_seqlens is None else list(zip(w.cu_seqlens[:-1], w.cu_seqlens[1:]))
-    for b in range(w.B):
-        for (a, e) in seqs:
-            n = e - a
-            i = torch.arange(n, device=device)[:, None]
-            j = torch.arange(n, device=device)[None, :]
-            vis = torch.ones(n, n, dtype=torch.bool, device=device)
-            if w.causal or w.window > 0:
-                vis &= j <= i
-            if w.window > 0:
-                vis &= j > i - w.window
-            for h in range(w.HQ):
-                Q = tq[b, a:e, h].float()
-                K = tk[b, a:e, h // G].float()
-                V = tv[b, a:e, h // G].float()
-                s = (Q @ K.T) * w.sm_scale
-                s = s.masked_fill(~vis, float("-inf"))
-                l = torch.logsumexp(s, dim=1)
-                o[b, a:e, h] = (torch.exp(s - l[:, None]) @ V).to(tdt)
-                lse[b, h, a:e] = l
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=device) if w.cu_seqlens else None
+    ws = torch.empty(256, dtype=torch.uint8, device=device)
+    o, lse = ab.forward(tq, tk, tv, w.sm_scale, w.causal, w.window, cu, workspace=ws)
+    ab.check_error(ws)
     return tq, tk, tv, o, tdo, lse
+
+
+def time_forward(w, tensors, steps, warmup, device, flush_bytes=256 << 20):
+    """The forward (attn_fwd_gqa) timed alone: events around each call, L2
+    flushed before each."""
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    tq, tk, tv, to, tdo, lse, cu = tensors
+    o, l_ = torch.empty_like(to), torch.empty_like(lse)
+    ws = torch.empty(256, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev):
+        ev[0].record(stream)
+        ab.attn_fwd_gqa(tq, tk, tv, o, l_, ws, w.sm_scale, w.causal, w.window, cu, stream)
+        ev[1].record(stream)
+
+    per = _timed_steps(step, steps, warmup, device, stream, ws, 2, flush_bytes, 1)
+    ts = [e[0].elapsed_time(e[1]) for e in per]
+    return {"ms": float(np.mean(ts)), "ms_pct": _pct(ts)}
 
 
 def gpu_sparse_inputs(w, device):
@@ -331,7 +336,9 @@ def time_dense(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
 
     per = _timed_steps(step, steps, warmup, device, stream, ws, 2, flush_bytes, world)
     per_st = _timed_steps(staged, steps, warmup, device, stream, ws, 4, flush_bytes, world)
-    return _stage_times(per, per_st) | {"tensors": (tq, tk, tv, to, tdo, lse, cu)}
+    tensors = (tq, tk, tv, to, tdo, lse, cu)
+    fwd = time_forward(w, tensors, steps, warmup, device, flush_bytes)
+    return _stage_times(per, per_st) | {"tensors": tensors, "forward": fwd}
 
 
 def time_sparse(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
@@ -627,6 +634,17 @@ def describe(w, r, pk, pk_kind, world=1):
             kname, src = f"dense128_bwd_kernel<{w.dtype}>", _os.path.join(csrc, "dense128_bwd.cu")
         else:
             kname, src = f"dense_bwd_kernel<{w.D},{w.dtype}>", _os.path.join(csrc, "dense_bwd.cu")
+        if "forward" in r:  # the forward that produced O and LSE, timed alone
+            fflops = flops / 2.5
+            fms = r["forward"]["ms"]
+            fach = fflops / (fms * 1e-3) / 1e12
+            fname = f"dense_fwd_kernel<{w.D},{w.dtype}>"
+            out["forward"] = {
+                "value": fach, "unit": "TFLOP/s", "ms": fms, "ms_pct": r["forward"]["ms_pct"], "flops": fflops,
+                "roofline": {"bound": "tensor", "achieved": fach, "peak": peak, "unit": "TFLOP/s",
+                             "frac": fach / peak, "kernel": fname, "kernel_ms": fms,
+                             "peak_kind": f"bf16 burst, {pk_kind}",
+                             "traffic": traffic_record(_os.path.join(csrc, "dense_fwd.cu"), fname + "@" + w.name)}}
     roof["traffic"] = traffic_record(src, kname + "@" + w.name)
     roof["peak_kind"] = f"{'bf16 burst' if roof['bound'] == 'tensor' else 'copy'}, {pk_kind}"
     roof["kernel"] = kname
@@ -699,6 +717,8 @@ def main():
     }
     if w.kind == "sparse":
         line["TFLOP/s"] = d["TFLOP/s"]
+    else:
+        line["forward"] = d.get("forward")
     if not args.no_e2e:
         e2e_ms, h2d, d2h = time_e2e(w, r["tensors"], max(3, args.steps // 4), device)
         per_step = d["value"] * r["ms_step"] / world  # this rank's units per step

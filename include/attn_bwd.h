@@ -165,6 +165,30 @@ ATTN_BWD_API attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const 
                                         void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv, void* workspace,
                                         size_t workspace_bytes, void* stream);
 
+/* The forward whose outputs the backward takes: O = softmax(scale Q K^T) V
+ * under the mask, and the natural-log LSE of every query row (the TileOPs
+ * page's backward op takes q, k, v, o, do, lse, "Summary"; the rows computed
+ * are the first half of its "Reference" program: masked scores, their softmax
+ * and log-sum-exp).  One CTA per two 128-row query tiles of one query head;
+ * tcgen05 MMAs with the scores and O in tensor memory, the row max updated
+ * lazily (O rescaled only when a row max grows by more than 2^8).
+ *   q, o : [B,S,HQ,D] 16-bit;  k, v : [B,Sk,HKV,D] 16-bit (Sk as for
+ *   attn_bwd_gqa);  lse : f32, lse[b*slse.b + h*slse.h + s*slse.s] (written);
+ *   o is written in the input dtype.  A query that sees no key gets O = 0 and
+ *   LSE = -inf.  Rows past cu_seqlens[num_seqs] are not written; their K/V
+ *   rows may hold anything (they are zeroed in shared memory before use).
+ *   D in {64, 128};  any G = HQ / HKV;  sm_scale finite and > 0.
+ *   workspace : at least 256 bytes, 16-byte aligned (the header of a backward
+ *   workspace serves); its error word is cleared by the call and
+ *   attn_bwd_check_error reports a kernel whose bounded wait ran out.
+ * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE
+ * before anything is queued; ATTN_ERR_LAUNCH if the runtime refuses. */
+ATTN_BWD_API attn_status_t attn_fwd_gqa(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
+                                        const void* v, attn_strides_t sv, int64_t B, int64_t S, int64_t HQ,
+                                        int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
+                                        const attn_mask_t* mask, void* o, attn_strides_t so, float* lse,
+                                        attn_strides_t slse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Multi-head attention: attn_bwd_gqa with HQ == HKV == H (the page's MHA op is
  * GQA with H_kv = H). */
 ATTN_BWD_API attn_status_t attn_bwd(const void* q, attn_strides_t sq, const void* k, attn_strides_t sk, const void* v,

@@ -24,7 +24,7 @@ def ab():
 
 def declared_symbols():
     src = open(os.path.join(ROOT, "include", "attn_bwd.h")).read()
-    return sorted(set(re.findall(r"ATTN_BWD_API\s+[\w\s\*]+?\b(attn_bwd\w*)\s*\(", src)))
+    return sorted(set(re.findall(r"ATTN_BWD_API\s+[\w\s\*]+?\b(attn_(?:bwd|fwd)\w*)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(ab):
@@ -35,6 +35,7 @@ def test_every_declared_symbol_is_exported(ab):
         assert hasattr(lib, n), n
     # and nothing else leaks out as a C symbol of ours
     assert "attn_bwd_gqa" in names and "attn_bwd_sparse" in names and "attn_bwd_preprocess" in names
+    assert "attn_fwd_gqa" in names
 
 
 def test_status_strings(ab):
@@ -344,3 +345,29 @@ def test_landing_and_noalloc_limits_return_before_any_launch(ab):
     assert host(scratch=fake + 16) == 1
     assert host(mask=ab._binding.Mask(1, -1, None, 0, 4096)) == 1   # key rows of another length
     assert lib.attn_bwd_host_scratch_size(2, 2048, 32, 32, 96, 4) == 0
+
+
+def test_forward_rejects_before_any_launch(ab):
+    """attn_fwd_gqa checks every argument before it touches the device."""
+    lib = ab.library()
+    S, M = ab._binding.Strides, ab._binding.Mask
+    fake = 1 << 20
+    good = S(2048 * 32 * 128, 32 * 128, 128)
+    lse = S(32 * 2048, 1, 2048)
+
+    def fwd(q=fake, o=fake, lse_=fake, ws=fake, ws_bytes=256, D=128, HQ=32, HKV=32, B=2, dtype=0, scale=0.1,
+            mask=M(1, -1, None, 0), sq=good):
+        return lib.attn_fwd_gqa(q, sq, fake, good, fake, good, B, 2048, HQ, HKV, D, dtype, scale, ctypes.byref(mask),
+                                o, good, lse_, lse, ws, ws_bytes, None)
+
+    assert fwd(q=None) == 1 and fwd(o=None) == 1 and fwd(lse_=None) == 1 and fwd(ws=None) == 1
+    assert fwd(q=fake + 2) == 1 and fwd(lse_=fake + 2) == 1
+    assert fwd(sq=S(0, 0, 0)) == 1
+    assert fwd(HQ=6, HKV=4) == 1
+    assert fwd(scale=0.0) == 1 and fwd(scale=-0.1) == 1 and fwd(scale=float("nan")) == 1
+    assert fwd(D=96) == 2 and fwd(dtype=7) == 2
+    assert fwd(ws_bytes=128) == 3
+    assert fwd(mask=M(1, 0, None, 0)) == 1
+    assert fwd(mask=M(1, -1, fake, 3)) == 1                  # varlen with B > 1
+    assert fwd(B=1, mask=M(1, -1, fake, 3, 100)) == 1         # a key length with packed sequences
+    assert fwd(mask=M(1, -1, None, 0, -1)) == 1
