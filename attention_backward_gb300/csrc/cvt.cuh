@@ -35,6 +35,15 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
   }
 }
 
+// The rounding residuals of a pair packed by pack2 (``hi``), rounded and packed
+// the same way: a + b's 16-bit hi pair plus this lo pair carries about 16
+// significant bits of each value.
+template <bool BF16>
+__device__ __forceinline__ uint32_t lo_pair(float a, float b, uint32_t hi) {
+  const float2 h = unpack2<BF16>(hi);
+  return pack2<BF16>(a - h.x, b - h.y);
+}
+
 // 2^x on the multi-function unit (MUFU.EX2), flush-to-zero.
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -44,6 +44,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 // the register split below needs the bounded waits' slow paths inlined
 #define AB_INLINE_WAITS 1
 #include "common.cuh"
@@ -132,7 +134,7 @@ enum Bar : int {
 };
 static_assert(NUM_BARS <= NBAR, "barrier storage");
 
-template <bool BF16>
+template <bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_constant__ DenseMaps maps,
                                                                   const DenseParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
   TileInfo* ring = reinterpret_cast<TileInfo*>(sm + OFF_RING);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 8);
+  // per step parity: gs + 1 when a softmax warp of step gs saw a P above kSplitP (bf16)
+  volatile uint32_t* split_flag = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC + 16);
   float* s_lse = reinterpret_cast<float*>(sm + OFF_LSE);
   float* s_delta = reinterpret_cast<float*>(sm + OFF_DELTA);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    split_flag[0] = split_flag[1] = 0u;
     for (int i = 0; i < ST; ++i) {
       mbar_init(&bars[FULL0 + i], 2);
       mbar_init(&bars[FULLD0 + i], 1);
@@ -480,6 +485,19 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_w(tmem + T_DK, tmem + T_S + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + so + sdesc_step(kk * 2048), IDESC_KV,
                    j > 0 || kk > 0);
+        if constexpr (SPLIT) {
+          // a step with a large P adds the rounding residuals of P and dS (their
+          // pairs sit in the dP^T columns, which the dQ below overwrites after)
+          // (queries 16kk .. 16kk + 15: P_lo pairs at dP^T column 16kk, dS_lo at 16kk + 8)
+          if (split_flag[gs & 1] == gs + 1) {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts_w(tmem + T_DV, tmem + T_DP + kk * 16, dO_mn + so + sdesc_step(kk * 2048), IDESC_KV, 1u);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts_w(tmem + T_DK, tmem + T_DP + kk * 16 + 8, dQ_mn + so + sdesc_step(kk * 2048), IDESC_KV, 1u);
+          }
+        }
         mma_commit_w(&bars[S_FREE]);
         // ---- dQ = dS K over the 128 key rows (A = dS MN-major in two 64-query blocks, B = K MN-major),
         // into the dP^T columns (the softmax warps read dP before publishing dS)
@@ -572,13 +590,25 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           }
         }
         // P^T pairs go into the first half of this warpgroup's own S^T columns,
-        // which only this warp's lanes read (and its loads have completed)
+        // which only this warp's lanes read (and its loads have completed); bf16
+        // keeps the largest rounded P of each half-word lane (P >= 0, so the
+        // 16-bit patterns order as unsigned integers)
+        uint32_t pmax2 = 0u;
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t w[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
+          for (int c = 0; c < 16; ++c) {
+            w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
+            if constexpr (SPLIT) pmax2 = __vmaxu2(pmax2, w[c]);
+          }
           tmem_st16(sb + wg * HALF + ch * 16, w);
+        }
+        // bf16: does this warp's part of the step need the rounding residuals?
+        bool big = false;
+        if constexpr (SPLIT) {
+          big = __any_sync(0xffffffffu, __vcmpgtu2(pmax2, kSplitPBf16x2) != 0u);
+          if (big && lane == 0) split_flag[gs & 1] = gs + 1;
         }
         tmem_st_wait();
         tc_fence_before();
@@ -590,30 +620,75 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DS_SFREE], (gs - 1) & 1, wc, kErrWaitDSFree))) break;
         tc_fence_after();
         uint8_t* dsb = sm + OFF_DS + wg * DS_BLOCK;
-        // both halves of this warpgroup's dP^T columns in flight at once
-        uint32_t dr[HALF];
-        tmem_ld32(tmem + lane_off + T_DP + wg * HALF, dr);
-        tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t dsw[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const int cc = ch * 32 + c;
-            const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
-            dsw[c / 2] = pack2<BF16>(pv[cc] * (__uint_as_float(dr[cc]) - dl.x),
-                                     pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y));
-            dsw[c / 2 + 1] = pack2<BF16>(pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z),
-                                         pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w));
+        // bf16: the step takes the rounding residuals if any softmax warp saw a
+        // large P (P_READY completes once all eight have flagged or not; the flag
+        // of step gs is rewritten only at step gs + 2)
+        bool split = big;
+        if constexpr (SPLIT) {
+          if (!split) {
+            if (!(ok = mbar_wait_warp(&bars[P_READY], gs & 1, wc, kErrWaitP))) break;
+            split = split_flag[gs & 1] == gs + 1;
           }
-          // dS^T pairs into the second half of this warpgroup's S^T columns, and dS
-          // as the MN-major A operand of dQ: 64-query block wg, row = key, 16-byte chunks 4ch..4ch+3
-          tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
+        }
+        // dS for 16 queries at a time: dS^T pairs into the second half of this
+        // warpgroup's S^T columns and dS as the MN-major A operand of dQ (64-query
+        // block wg, row = key, two 16-byte chunks).  A step with the residuals
+        // also writes those of P^T and dS^T of each 16 queries into 16 of this
+        // warpgroup's dP^T columns once they are loaded (P_lo pairs, then dS_lo
+        // pairs; read by the residual MMAs, then overwritten by this step's dQ),
+        // and loads the second half of its dP^T columns only when it reaches
+        // them, which keeps the residuals within the warp's registers.
+        auto ds_stage = [&](auto split_c) {
+          constexpr bool SPLIT = decltype(split_c)::value;
+          uint32_t dr[HALF];
+          tmem_ld32(tmem + lane_off + T_DP + wg * HALF, dr);
+          if constexpr (!SPLIT) tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
+          tmem_ld_wait();
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            *reinterpret_cast<uint4*>(dsb + sw128_offset(row, ch * 4 + c4)) =
-                make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+          for (int g = 0; g < HALF / 16; ++g) {
+            if constexpr (SPLIT) {
+              if (g == HALF / 32) {
+                tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
+                tmem_ld_wait();
+              }
+            }
+            uint32_t dsw[8], plo[8], dsl[8];
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+              const int cc = g * 16 + c;
+              const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
+              const float d0 = pv[cc] * (__uint_as_float(dr[cc]) - dl.x);
+              const float d1 = pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y);
+              const float d2 = pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z);
+              const float d3 = pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w);
+              dsw[c / 2] = pack2<BF16>(d0, d1);
+              dsw[c / 2 + 1] = pack2<BF16>(d2, d3);
+              if constexpr (SPLIT) {
+                dsl[c / 2] = lo_pair<BF16>(d0, d1, dsw[c / 2]);
+                dsl[c / 2 + 1] = lo_pair<BF16>(d2, d3, dsw[c / 2 + 1]);
+                plo[c / 2] = lo_pair<BF16>(pv[cc], pv[cc + 1], pack2<BF16>(pv[cc], pv[cc + 1]));
+                plo[c / 2 + 1] = lo_pair<BF16>(pv[cc + 2], pv[cc + 3], pack2<BF16>(pv[cc + 2], pv[cc + 3]));
+              }
+            }
+            tmem_st8(sb + wg * HALF + HALF / 2 + g * 8, dsw);
+#pragma unroll
+            for (int c4 = 0; c4 < 2; ++c4)
+              *reinterpret_cast<uint4*>(dsb + sw128_offset(row, g * 2 + c4)) =
+                  make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+            if constexpr (SPLIT) {
+              const uint32_t lo_col = tmem + lane_off + T_DP + wg * HALF + g * 16;
+              tmem_st8(lo_col, plo);
+              tmem_st8(lo_col + 8, dsl);
+            }
+          }
+        };
+        if constexpr (SPLIT) {
+          if (split)
+            ds_stage(std::true_type{});
+          else
+            ds_stage(std::false_type{});
+        } else {
+          ds_stage(std::false_type{});
         }
         fence_proxy_async_smem();
         tmem_st_wait();
@@ -723,9 +798,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool SPLIT>
 cudaError_t launch_t(const DenseParams& p, const DenseMaps& m, int grid, cudaStream_t st) {
-  auto kern = dense128_bwd_kernel<BF16>;
+  auto kern = dense128_bwd_kernel<BF16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, THREADS, SMEM, st>>>(m, p);
@@ -735,7 +810,8 @@ cudaError_t launch_t(const DenseParams& p, const DenseMaps& m, int grid, cudaStr
 }  // namespace
 
 cudaError_t launch_dense128(const DenseParams& p, const DenseMaps& m, bool bf16, int grid, cudaStream_t st) {
-  return bf16 ? launch_t<true>(p, m, grid, st) : launch_t<false>(p, m, grid, st);
+  if (!bf16) return launch_t<false, false>(p, m, grid, st);
+  return p.G > kSplitMinGroup ? launch_t<true, true>(p, m, grid, st) : launch_t<true, false>(p, m, grid, st);
 }
 
 }  // namespace ab

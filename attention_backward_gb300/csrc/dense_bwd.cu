@@ -45,6 +45,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 // the register split below needs the bounded waits' slow paths inlined
 #define AB_INLINE_WAITS 1
 #include "common.cuh"
@@ -137,7 +139,7 @@ enum Bar : int {
 };
 static_assert(NUM_BARS <= Cfg<64>::NBAR, "barrier storage");
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __grid_constant__ DenseMaps maps, const DenseParams p) {
   using C = Cfg<D>;
   constexpr int BM = C::BM, BN = C::BN, ST = C::STAGES, kPrefetch = C::PREFETCH;
@@ -146,6 +148,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   TileInfo* ring = reinterpret_cast<TileInfo*>(sm + C::OFF_RING);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
+  // per step parity: gs + 1 when a softmax warp of step gs saw a P above kSplitP (bf16)
+  volatile uint32_t* split_flag = reinterpret_cast<volatile uint32_t*>(sm + C::OFF_MISC + 16);
   float* s_lse = reinterpret_cast<float*>(sm + C::OFF_LSE);
   float* s_delta = reinterpret_cast<float*>(sm + C::OFF_DELTA);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    split_flag[0] = split_flag[1] = 0u;
     for (int i = 0; i < ST; ++i) {
       mbar_init(&bars[FULL0 + i], 2);  // producer: expect_tx arrival + arrival after LSE/delta stores
       mbar_init(&bars[EMPTY0 + i], 1);
@@ -470,8 +475,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           mma_ts_w(tmem + C::T_DV, sb + pair_col(kk * 16, BN / 2), dO_mn + qo + sdesc_step(kk * 2048), IDESC_KV,
                    j > 0 || kk > 0);
         // ---- dP^T of the next step, as soon as this step's dP^T has been loaded
-        if (j + 1 < n) {
-          if (!(ok = mbar_wait_warp(&bars[DP_FREE], cur & 1, wc, kErrWaitDP))) break;
+        // (bf16: after this step's residual MMAs, which read residual pairs that
+        // the softmax warps wrote into the dP^T columns)
+        auto issue_next_dp = [&]() -> bool {
+          if (j + 1 >= n) return true;
+          if (!mbar_wait_warp(&bars[DP_FREE], cur & 1, wc, kErrWaitDP)) return false;
           tc_fence_after();
           const uint64_t qn = sdesc_step(((cur + 1) % ST) * C::Q_TILE);
 #pragma unroll
@@ -481,7 +489,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             mma_ss_w(tmem + C::T_DP, dV_kmaj + ko, dO_kmaj + qn + qk, IDESC_S, kk > 0);
           }
           mma_commit_w(&bars[DP_FULL]);
-        }
+          return true;
+        };
+        // bf16 steps with the residuals (flagged by the softmax warps before P_READY)
+        bool split = false;
+        if constexpr (SPLIT) split = split_flag[cur & 1] == cur + 1;
+        if (!split && !(ok = issue_next_dp())) break;
         // ---- dK += dS^T Q (B = Q as [N = D] x [K = queries], MN-major)
         if (!(ok = mbar_wait_warp(&bars[DS_READY], cur & 1, wc, kErrWaitDS))) break;
         tc_fence_after();
@@ -489,6 +502,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_w(tmem + C::T_DK, sb + pair_col(kk * 16, BN / 2) + BN / 4, dQ_mn + qo + sdesc_step(kk * 2048),
                    IDESC_KV, j > 0 || kk > 0);
+        if constexpr (SPLIT) {
+          // a step with a large P adds the rounding residuals of P and dS (queries
+          // 16kk .. 16kk + 15: P_lo pairs at dP^T column 16kk, dS_lo at 16kk + 8)
+          if (split) {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts_w(tmem + C::T_DV, tmem + C::T_DP + kk * 16, dO_mn + qo + sdesc_step(kk * 2048), IDESC_KV, 1u);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts_w(tmem + C::T_DK, tmem + C::T_DP + kk * 16 + 8, dQ_mn + qo + sdesc_step(kk * 2048), IDESC_KV,
+                       1u);
+            if (!(ok = issue_next_dp())) break;
+          }
+        }
         // dQ overwrites this step's S^T buffer, which dV and dK read: MMAs issued
         // by one thread run in issue order, so no wait is needed in between
         const uint32_t dq_cols = sb;
@@ -587,13 +614,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           }
         }
         // P^T pairs go into the first half of this warpgroup's own S^T columns,
-        // which only this warp's lanes read (and its loads have completed)
+        // which only this warp's lanes read (and its loads have completed); bf16
+        // keeps the largest rounded P of each half-word lane (P >= 0, so the
+        // 16-bit patterns order as unsigned integers)
+        uint32_t pmax2 = 0u;
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t w[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
+          for (int c = 0; c < 16; ++c) {
+            w[c] = pack2<BF16>(pv[ch * 32 + 2 * c], pv[ch * 32 + 2 * c + 1]);
+            if constexpr (SPLIT) pmax2 = __vmaxu2(pmax2, w[c]);
+          }
           tmem_st16(sb + wg * HALF + ch * 16, w);
+        }
+        // bf16: does this warp's part of the step need the rounding residuals?
+        bool big = false;
+        if constexpr (SPLIT) {
+          big = __any_sync(0xffffffffu, __vcmpgtu2(pmax2, kSplitPBf16x2) != 0u);
+          if (big && lane == 0) split_flag[gs & 1] = gs + 1;
         }
         tmem_st_wait();
         tc_fence_before();
@@ -606,35 +645,99 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             !(ok = mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree)))
           break;
         tc_fence_after();
-        // both halves of this warpgroup's dP^T columns in flight at once; the next
-        // step's dP^T may overwrite them as soon as they are loaded
-        uint32_t dr[HALF];
-        tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF, dr);
-        tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + 32, dr + 32);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[DP_FREE]);
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t dsw[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const int cc = ch * 32 + c;
-            const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
-            dsw[c / 2] = pack2<BF16>(pv[cc] * (__uint_as_float(dr[cc]) - dl.x),
-                                     pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y));
-            dsw[c / 2 + 1] = pack2<BF16>(pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z),
-                                         pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w));
+        // bf16: the step takes the rounding residuals if any softmax warp saw a
+        // large P (its P_READY completes once all eight have flagged or not; the
+        // flag of step gs is rewritten only at step gs + 2)
+        bool split = big;
+        if constexpr (SPLIT) {
+          if (!split) {
+            if (!(ok = mbar_wait_warp(&bars[P_READY0 + (gs & 1)], (gs >> 1) & 1, wc, kErrWaitP))) break;
+            split = split_flag[gs & 1] == gs + 1;
           }
-          // dS^T pairs into the second half of this warpgroup's S^T columns
-          tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
-          // dS as the MN-major A operand of dQ: 64-query block wg, row = key, chunks 4ch .. 4ch+3
-          uint8_t* base = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES + wg * (BM * 128);
+        }
+        uint8_t* const dsbase = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES + wg * (BM * 128);
+        // dS for 16 queries at a time: dS^T pairs into the second half of this
+        // warpgroup's S^T columns, dS as the MN-major A operand of dQ (64-query
+        // block wg, row = key, two 16-byte chunks).  The next step's dP^T may
+        // overwrite this warpgroup's dP^T columns once they are loaded (DP_FREE)
+        // - except in a step with the residuals, which writes those of P^T and
+        // dS^T of each 16 queries into 16 of these columns (P_lo pairs, then dS_lo
+        // pairs; the next dP^T is issued after the residual MMAs) and loads the
+        // second half only when it reaches it, keeping the residuals within the
+        // warp's registers.
+        auto ds_stage = [&](auto split_c) {
+          constexpr bool SPLIT = decltype(split_c)::value;
+          uint32_t dr[HALF];
+          tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF, dr);
+          if constexpr (!SPLIT) tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + 32, dr + 32);
+          tmem_ld_wait();
+          auto dp_loaded = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[DP_FREE]);
+          };
+          if constexpr (!SPLIT) {
+            dp_loaded();
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            *reinterpret_cast<uint4*>(base + sw128_offset(row, ch * 4 + c4)) =
-                make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t dsw[16];
+#pragma unroll
+              for (int c = 0; c < 32; c += 4) {
+                const int cc = ch * 32 + c;
+                const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
+                dsw[c / 2] = pack2<BF16>(pv[cc] * (__uint_as_float(dr[cc]) - dl.x),
+                                         pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y));
+                dsw[c / 2 + 1] = pack2<BF16>(pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z),
+                                             pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w));
+              }
+              tmem_st16(sb + wg * HALF + HALF / 2 + ch * 16, dsw);
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4)
+                *reinterpret_cast<uint4*>(dsbase + sw128_offset(row, ch * 4 + c4)) =
+                    make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < HALF / 16; ++g) {
+              if (g == HALF / 32) {
+                tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + 32, dr + 32);
+                tmem_ld_wait();
+                dp_loaded();
+              }
+              uint32_t dsw[8], plo[8], dsl[8];
+#pragma unroll
+              for (int c = 0; c < 16; c += 4) {
+                const int cc = g * 16 + c;
+                const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
+                const float d0 = pv[cc] * (__uint_as_float(dr[cc]) - dl.x);
+                const float d1 = pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y);
+                const float d2 = pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z);
+                const float d3 = pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w);
+                dsw[c / 2] = pack2<BF16>(d0, d1);
+                dsw[c / 2 + 1] = pack2<BF16>(d2, d3);
+                dsl[c / 2] = lo_pair<BF16>(d0, d1, dsw[c / 2]);
+                dsl[c / 2 + 1] = lo_pair<BF16>(d2, d3, dsw[c / 2 + 1]);
+                plo[c / 2] = lo_pair<BF16>(pv[cc], pv[cc + 1], pack2<BF16>(pv[cc], pv[cc + 1]));
+                plo[c / 2 + 1] = lo_pair<BF16>(pv[cc + 2], pv[cc + 3], pack2<BF16>(pv[cc + 2], pv[cc + 3]));
+              }
+              tmem_st8(sb + wg * HALF + HALF / 2 + g * 8, dsw);
+#pragma unroll
+              for (int c4 = 0; c4 < 2; ++c4)
+                *reinterpret_cast<uint4*>(dsbase + sw128_offset(row, g * 2 + c4)) =
+                    make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
+              const uint32_t lo_col = tmem + lane_off + C::T_DP + wg * HALF + g * 16;
+              tmem_st8(lo_col, plo);
+              tmem_st8(lo_col + 8, dsl);
+            }
+          }
+        };
+        if constexpr (SPLIT) {
+          if (split)
+            ds_stage(std::true_type{});
+          else
+            ds_stage(std::false_type{});
+        } else {
+          ds_stage(std::false_type{});
         }
         if (!ok) break;
         fence_proxy_async_smem();
@@ -734,9 +837,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 cudaError_t launch_dense_t(const DenseParams& p, const DenseMaps& m, int grid, cudaStream_t st) {
-  auto kern = dense_bwd_kernel<D, BF16>;
+  auto kern = dense_bwd_kernel<D, BF16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM, st>>>(m, p);
@@ -764,7 +867,9 @@ cudaError_t launch_dense(const DenseParams& p, const DenseMaps& m, bool bf16, in
   if (p.bn != kDenseBN) return cudaErrorInvalidValue;
   if (p.D == 128) return launch_dense128(p, m, bf16, grid, st);
   if (p.D != 64) return cudaErrorInvalidValue;
-  return bf16 ? launch_dense_t<64, true>(p, m, grid, st) : launch_dense_t<64, false>(p, m, grid, st);
+  if (!bf16) return launch_dense_t<64, false, false>(p, m, grid, st);
+  return p.G > kSplitMinGroup ? launch_dense_t<64, true, true>(p, m, grid, st)
+                              : launch_dense_t<64, true, false>(p, m, grid, st);
 }
 
 cudaError_t launch_selftest_timeout(int* err, uint64_t timeout_ns, cudaStream_t st) {

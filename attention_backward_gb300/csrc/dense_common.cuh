@@ -23,6 +23,22 @@ __host__ __device__ constexpr uint32_t pair_col(int q, int half) {
   return static_cast<uint32_t>((q / half) * half + (q % half) / 2);
 }
 
+// bf16 steps whose largest P exceeds this add the 16-bit rounding residuals of
+// P and dS through a second pair of dV / dK MMAs (dV += P_lo^T dO, dK +=
+// dS_lo^T Q).  P is rounded to the input dtype before the dV product, as the
+// TileOPs page's "Tiled" program does; with bf16's 8-bit significand the
+// rounding errors of large P (short causal rows) summed over a group's heads
+// exceed the bf16 tolerance, while steps whose P all stay at or below 1/8 keep
+// them well inside it (a bit-exact model of the rounding over group sizes up
+// to 16 puts the worst element at 0.34 of the tolerance).
+constexpr float kSplitP = 0.125f;
+constexpr uint32_t kSplitPBf16x2 = 0x3E003E00u;  // kSplitP as two bf16 patterns
+// The residuals are compiled into the bf16 kernels that serve groups of more
+// than this many query heads per KV head; up to 4 heads, the same model keeps
+// the plain 16-bit rounding within 0.76 of the tolerance, and those launches
+// run without the check (it costs the softmax warps a few percent).
+constexpr int kSplitMinGroup = 4;
+
 // (batch, KV head) pairs whose tiles are drawn together (dense batches).
 constexpr int kTileGroup = 8;
 

@@ -132,13 +132,16 @@ ATTN_BWD_API attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so,
                                   size_t workspace_bytes, void* stream);
 
 /* Group sizes G = HQ / HKV the dense path accepts: at most 16 query heads per
- * KV head in fp16 and at most 8 in bf16.  P is rounded to the input dtype
- * before dV += P^T dO (as the TileOPs page's "Tiled" program does); with bf16's
- * 8-bit significand the rounding errors of one key row, summed over more than
- * 8 heads of short causal rows, exceed the bf16 tolerance, so larger groups
- * are refused (ATTN_ERR_UNSUPPORTED) rather than served inexactly. */
+ * KV head in either dtype (larger groups return ATTN_ERR_UNSUPPORTED).  P and
+ * dS are rounded to the input dtype before the dV and dK products, as the
+ * TileOPs page's "Tiled" program does.  With bf16's 8-bit significand the
+ * rounding errors of large P (short causal rows), summed over the group's
+ * heads, would exceed the bf16 tolerance from G = 8 on; so for bf16 groups of
+ * more than 4 heads a step whose largest P exceeds 1/8 also adds the 16-bit
+ * rounding residuals of P and dS through a second pair of dV / dK products.
+ * Steps of long rows, whose P stay small, run without them. */
 #define ATTN_BWD_MAX_GROUP_F16 16
-#define ATTN_BWD_MAX_GROUP_BF16 8
+#define ATTN_BWD_MAX_GROUP_BF16 16
 
 /* The whole dense backward of grouped-query attention in one call: the
  * TileOPs page's three launches behind one op call ("Summary": preprocess,

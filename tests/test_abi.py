@@ -166,9 +166,9 @@ def test_argument_errors_return_before_any_launch(ab):
     assert main(mask=ab._binding.Mask(1, 0, None, 0)) == 1            # window of zero
     assert main(mask=ab._binding.Mask(1, -1, fake, 3)) == 1           # varlen with B > 1
     assert main(scale=float("nan")) == 1
-    # group sizes beyond the precision limits: 16 heads per KV head in fp16, 8 in bf16
+    # group sizes beyond the limit: 16 heads per KV head in either dtype
     assert main(H=32, HKV=1) == 2
-    assert main(H=16, HKV=1, dtype=1) == 2
+    assert main(H=32, HKV=1, dtype=1) == 2
     # preprocess: bad head dim, workspace too small
     assert lib.attn_bwd_preprocess(fake, good, fake, good, fake, S(64, 1, 2048), 2, 2048, 32, 12, 128, 0, 0,
                                    fake, 1 << 30, None) == 1
@@ -232,7 +232,7 @@ BAD_CALLS = [
     ("head dim 96", dict(D=96), 2),
     ("dtype 7", dict(dtype=7), 2),
     ("G = 32 fp16", dict(HQ=32, HKV=1), 2),
-    ("G = 16 bf16", dict(HQ=32, HKV=2, dtype=1), 2),
+    ("G = 32 bf16", dict(HQ=32, HKV=1, dtype=1), 2),
 ]
 
 

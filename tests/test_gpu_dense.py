@@ -26,12 +26,13 @@ SMALL = [
     inputs.scaled(C1, name="s2_noncausal", S=2, causal=False),
     inputs.scaled(C1, name="s129_bf16", S=129, dtype="bf16"),
     inputs.scaled(C1, name="s127_b3", S=127, B=3, HQ=1, HKV=1),
-    # every group size the ABI accepts, in both dtypes: G in {1, 2, 4, 8, 16} for
-    # fp16 and {1, 2, 4, 8} for bf16, plus group sizes that are not powers of two.
-    # bf16 with G > 8 is refused (test_group_size_limits_are_enforced): the
-    # rounding of P to 16 bits before the dV product (as the page's Tiled
-    # program does) alone exceeds the bf16 tolerance there on short causal rows.
+    # group sizes in both dtypes, powers of two and not (every accepted G has a
+    # case of its own in EVERY_G below).  bf16 groups of 8 and 16 on short causal
+    # rows need the rounding residuals of P and dS that the kernels add on steps
+    # with a large P: without them the 16-bit rounding of P before the dV
+    # product (as the page's Tiled program does) exceeds the bf16 tolerance.
     inputs.scaled(C3, name="gqa_g4_s384", S=384, HQ=8, HKV=2),
+    inputs.scaled(C3, name="gqa_g16_s300_causal_bf16", S=300, HQ=16, HKV=1, causal=True),
     inputs.scaled(C3, name="gqa_g16_s300_causal_f16", S=300, HQ=16, HKV=1, causal=True, dtype="f16"),
     inputs.scaled(C3, name="gqa_g8_s300_causal_bf16", S=300, HQ=8, HKV=1, causal=True),
     inputs.scaled(C3, name="gqa_g8_s300_causal_f16", S=300, HQ=16, HKV=2, causal=True, dtype="f16"),
@@ -110,11 +111,11 @@ def test_unequal_query_and_key_lengths_match_oracle(w):
 
 
 # Every group size the ABI accepts, one small causal case each: G = 1..16 in
-# fp16, G = 1..8 in bf16, alternating head dims 64 and 128, two KV heads.
+# both dtypes, alternating head dims 64 and 128, two KV heads.
 EVERY_G = [
     inputs.scaled(C3, name=f"every_g{g}_{dt}_d{d}", S=200, HQ=2 * g, HKV=2, D=d, Dv=d, causal=True, dtype=dt,
                   seed=20260100 + g)
-    for dt, gmax in (("f16", 16), ("bf16", 8)) for g in range(1, gmax + 1) for d in ((64, 128)[g % 2],)
+    for dt, gmax in (("f16", 16), ("bf16", 16)) for g in range(1, gmax + 1) for d in ((64, 128)[g % 2],)
 ]
 
 
@@ -145,14 +146,13 @@ def test_split_launches_match_one_call():
 
 
 def test_group_size_limits_are_enforced():
-    """Group sizes past the precision limits are refused with
-    ATTN_ERR_UNSUPPORTED before anything runs: bf16 beyond 8 query heads per
-    KV head, fp16 beyond 16."""
+    """Group sizes past the limit (16 query heads per KV head) are refused
+    with ATTN_ERR_UNSUPPORTED before anything runs, in both dtypes."""
     import torch
 
     import attention_backward_gb300 as ab
 
-    for dt, hq in ((torch.bfloat16, 16), (torch.float16, 32)):
+    for dt, hq in ((torch.bfloat16, 32), (torch.float16, 32)):
         q = torch.zeros(1, 128, hq, 128, dtype=dt, device="cuda")
         kv = torch.zeros(1, 128, 1, 128, dtype=dt, device="cuda")
         lse = torch.zeros(1, hq, 128, dtype=torch.float32, device="cuda")
