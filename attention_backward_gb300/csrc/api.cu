@@ -317,16 +317,19 @@ attn_status_t setup_fwd(FwdSetup* s, const void* q, attn_strides_t sq, const voi
   p.o = static_cast<uint8_t*>(o), p.so_b = so.b, p.so_s = so.s, p.so_h = so.h;
   p.lse = lse, p.sl_b = slse.b, p.sl_s = slse.s, p.sl_h = slse.h;
   p.err = &static_cast<WsHeader*>(workspace)->err;
+  p.unit_counter = &static_cast<WsHeader*>(workspace)->tile_counter;
   p.timeout_ns = wait_limit_ns();
   s->bf16 = dtype == ATTN_DT_BF16;
-  s->grid = static_cast<int>(units);
+  // persistent CTAs, one per SM, draw units from the counter
+  s->grid = static_cast<int>(units < sm_count() ? units : sm_count());
   s->workspace = workspace;
   return ATTN_OK;
 }
 
 attn_status_t run_fwd(const FwdSetup& s, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the error word starts clear; the kernel records the first wait that ran out
+  // the error word and the unit counter start clear; the kernel records the
+  // first wait that ran out
   if (cudaMemsetAsync(s.workspace, 0, kHeaderBytes, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return launch_status(launch_fwd(s.p, s.m, s.bf16, s.grid, st));
 }

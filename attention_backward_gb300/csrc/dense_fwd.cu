@@ -6,7 +6,8 @@
 // "Reference" program's first half (scores, masked softmax, LSE) is what each
 // row computes here.
 //
-// Structure (one CTA per unit of two 128-row query tiles of one query head):
+// Structure (persistent CTAs, one per SM, each walking units of two 128-row
+// query tiles of one query head):
 //
 //   S_w  = Q_w K_j^T         tensor core, M = 128 queries, N = 128 keys, K = D
 //   m    = running row max of S_w * scale * log2(e) (lazily updated, below)
@@ -58,8 +59,9 @@ constexpr int BQ = 128;  // query rows per tile
 constexpr int BK = 128;  // keys per block
 constexpr int THREADS = 12 * 32;
 // launched at 168 registers a thread (12 warps), re-split per warpgroup: the
-// two softmax warpgroups hold a row of 128 scores each
-constexpr uint32_t REG_SOFT = 216, REG_CTL = 72;
+// two softmax warpgroups hold a row of 128 scores each; the control warpgroup
+// keeps the unit walk and the barrier phases of the persistent loop
+constexpr uint32_t REG_SOFT = 208, REG_CTL = 88;
 static_assert(2 * REG_SOFT + REG_CTL == 3 * 168, "register split must equal the launch's registers");
 constexpr float kRescaleLog2 = 8.f;  // rescale once a row max grows past 2^8
 
@@ -81,13 +83,17 @@ struct FwdCfg {
 
 enum FwdBar : int {
   Q_FULL = 0,
-  K_FULL0 = 1,        // ST stages
+  Q_EMPTY,            // every S MMA of the unit has completed: the Q tiles may be reloaded
+  K_FULL0,            // ST stages
   V_FULL0 = K_FULL0 + 4,
   KV_EMPTY0 = V_FULL0 + 4,
   S_FULL0 = KV_EMPTY0 + 4,  // per tile
   P_READY0 = S_FULL0 + 2,   // per tile: 4 softmax warps stored P
   O_DONE0 = P_READY0 + 2,   // per tile: the tile's P V MMAs issued so far completed
-  TAIL = O_DONE0 + 2,
+  O_FREE0 = O_DONE0 + 2,    // per tile: 4 softmax warps read the unit's O rows
+  UNIT_FULL0 = O_FREE0 + 2,   // 2 ring slots: the producer published a unit index
+  UNIT_EMPTY0 = UNIT_FULL0 + 2,  // 2 ring slots: the MMA warp and the 8 softmax warps read it
+  TAIL = UNIT_EMPTY0 + 2,
   DRAIN,
   NUM_FWD_BARS
 };
@@ -129,6 +135,7 @@ __device__ __forceinline__ void key_block_range(int q0, int qlen, int klen, int 
 __device__ __forceinline__ FwdUnit decode_unit(int u, const FwdParams& p) {
   FwdUnit t{};
   t.valid = 0;
+  if (u < 0) return t;  // the end-of-work marker
   int pair = 0;
   if (p.cu_seqlens == nullptr) {
     const int np = (p.S + 2 * BQ - 1) / (2 * BQ);
@@ -168,6 +175,36 @@ __device__ __forceinline__ FwdUnit decode_unit(int u, const FwdParams& p) {
   return t;
 }
 
+// The blocks [J0, J1) of a unit that some tile sees (J0 == J1: none).
+struct UnitSpan {
+  bool has[2];
+  int J0, J1;
+};
+
+__device__ __forceinline__ UnitSpan unit_span(const FwdUnit& u) {
+  UnitSpan s;
+  s.J0 = 0x7fffffff;
+  s.J1 = 0;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    s.has[w] = u.lo[w] < u.hi[w];
+    if (s.has[w]) {
+      s.J0 = imin(s.J0, u.lo[w]);
+      s.J1 = imax(s.J1, u.hi[w]);
+    }
+  }
+  if (s.J1 == 0) s.J0 = 0;
+  return s;
+}
+
+// Persistent: each CTA's producer draws units, longest first, from a counter
+// in the workspace header (cleared by the host before the launch) and
+// publishes each draw to the other roles through a two-slot ring in shared
+// memory; a draw past the last unit ends every role.  Barrier phases run on
+// across units (K/V stages by a block counter, the S / P / O barriers of a
+// tile by that tile's block counter), and two barriers hand the shared Q tiles
+// (Q_EMPTY: every S MMA of the unit has completed) and a tile's O accumulator
+// (O_FREE: its softmax warps have read O) to the next unit.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_constant__ FwdMaps maps,
                                                                const FwdParams p) {
@@ -177,30 +214,19 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
+  volatile int* ring = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 16);  // 2 unit indices
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if ((smem_u32(sm) & 1023u) != 0) {  // the swizzled tiles need an aligned base
     if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrAlign);
     return;
   }
-  const FwdUnit u = decode_unit(blockIdx.x, p);
-  if (!u.valid) return;  // a draw past the last unit (the grid is sized for the worst case)
-  bool has[2];
-  int J0 = 0x7fffffff, J1 = 0;
-#pragma unroll
-  for (int w = 0; w < 2; ++w) {
-    has[w] = u.lo[w] < u.hi[w];
-    if (has[w]) {
-      J0 = imin(J0, u.lo[w]);
-      J1 = imax(J1, u.hi[w]);
-    }
-  }
-  if (J1 == 0) J0 = 0;  // no tile sees a key: the softmax warps write the empty rows
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(&bars[Q_FULL], 1);
+    mbar_init(&bars[Q_EMPTY], 1);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&bars[K_FULL0 + i], 1);
       mbar_init(&bars[V_FULL0 + i], 1);
@@ -210,6 +236,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
       mbar_init(&bars[S_FULL0 + w], 1);
       mbar_init(&bars[P_READY0 + w], 4);
       mbar_init(&bars[O_DONE0 + w], 1);
+      mbar_init(&bars[O_FREE0 + w], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[UNIT_FULL0 + i], 1);
+      mbar_init(&bars[UNIT_EMPTY0 + i], 9);
     }
     mbar_init(&bars[TAIL], 1);
     mbar_init(&bars[DRAIN], 1);
@@ -234,79 +265,110 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
     }
   };
 
+  // the uc-th unit of this CTA (consumers): waits for the producer's draw,
+  // hands the slot back, decodes; invalid once the draws are exhausted
+  auto next_unit = [&](uint32_t uc, bool* okp) -> FwdUnit {
+    const uint32_t slot = uc & 1;
+    FwdUnit u{};
+    u.valid = 0;
+    if (!(*okp = mbar_wait_warp(&bars[UNIT_FULL0 + slot], (uc >> 1) & 1, wc, kErrWaitTile))) return u;
+    const int t = ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[UNIT_EMPTY0 + slot]);
+    return decode_unit(t, p);
+  };
+
   if (warp >= 8) {
     setmaxnreg_dec<REG_CTL>();
-    if (warp == 8 && J1 > J0) {
+    if (warp == 8) {
       // ============================================================ producer
-      const int kvh = u.h / p.G;
-      int q_pend = -1, tail_pend = -1, issued = 0;
-      uint32_t tail_ph = 0;
+      int q_pend = -1, tail_pend = -1;
+      uint32_t qc = 0, kc = 0, tail_ph = 0;
       bool ok = true;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[Q_FULL], (has[0] + has[1]) * C::TILE);
-        for (int w = 0; w < 2; ++w) {
-          if (!has[w]) continue;
-#pragma unroll
-          for (int s = 0; s < C::NSLAB; ++s)
-            tma_load_4d(sm + C::OFF_Q + w * C::TILE + s * C::SLAB, &maps.q, &bars[Q_FULL], s * 64, u.h,
-                        u.seq_start + u.q0 + w * BQ, u.b);
-        }
-      }
-      q_pend = 0;
       // key rows from tail0 on belong to no packed sequence and may hold anything
       const int rows = p.cu_seqlens ? p.S : p.Sk;
       const int tail0 = p.cu_seqlens ? clamp_pos(p.cu_seqlens[p.num_seqs], p.S) : p.Sk;
-      for (int j = J0; j < J1 && ok; ++j) {
-        const int i = j - J0, st = i % ST, n = i / ST;
-        if (n >= 1 && !(ok = mbar_wait_warp(&bars[KV_EMPTY0 + st], (n - 1) & 1, wc, kErrWaitStageEmpty))) break;
-        uint8_t* dk = sm + C::OFF_KV + 2 * st * C::TILE;
-        uint8_t* dv = dk + C::TILE;
-        const int pos = u.seq_start + j * BK;
-        int r0, r1;
-        tail_rows(pos, BK, tail0, rows, &r0, &r1);
-        if (r0 < r1) {
-          // loaded onto the producer's own barrier, the tail rows zeroed, then published
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[TAIL], 2 * C::TILE);
-#pragma unroll
-            for (int s = 0; s < C::NSLAB; ++s) {
-              tma_load_4d(dk + s * C::SLAB, &maps.k, &bars[TAIL], s * 64, kvh, pos, u.b);
-              tma_load_4d(dv + s * C::SLAB, &maps.v, &bars[TAIL], s * 64, kvh, pos, u.b);
-            }
-          }
-          tail_pend = tail_ph & 1;
-          if (!(ok = mbar_wait_warp(&bars[TAIL], tail_ph & 1, wc, kErrWaitTail))) break;
-          tail_pend = -1;
-          ++tail_ph;
-          zero_tile_rows(dk, C::NSLAB, C::SLAB, r0, r1, lane);
-          zero_tile_rows(dv, C::NSLAB, C::SLAB, r0, r1, lane);
-          if (lane == 0) {
-            mbar_arrive(&bars[K_FULL0 + st]);
-            mbar_arrive(&bars[V_FULL0 + st]);
-          }
-        } else if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[K_FULL0 + st], C::TILE);
-#pragma unroll
-          for (int s = 0; s < C::NSLAB; ++s)
-            tma_load_4d(dk + s * C::SLAB, &maps.k, &bars[K_FULL0 + st], s * 64, kvh, pos, u.b);
-          mbar_arrive_expect_tx(&bars[V_FULL0 + st], C::TILE);
-#pragma unroll
-          for (int s = 0; s < C::NSLAB; ++s)
-            tma_load_4d(dv + s * C::SLAB, &maps.v, &bars[V_FULL0 + st], s * 64, kvh, pos, u.b);
+      for (uint32_t uc = 0; ok; ++uc) {
+        const uint32_t slot = uc & 1;
+        if (uc >= 2 && !(ok = mbar_wait_warp(&bars[UNIT_EMPTY0 + slot], ((uc >> 1) - 1) & 1, wc, kErrWaitTile)))
+          break;
+        int t = 0;
+        if (lane == 0) t = atomicAdd(p.unit_counter, 1);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        const FwdUnit u = decode_unit(t, p);
+        if (lane == 0) {
+          ring[slot] = u.valid ? t : -1;
+          mbar_arrive(&bars[UNIT_FULL0 + slot]);
         }
-        issued = i + 1;
+        if (!u.valid) break;
+        const UnitSpan sp = unit_span(u);
+        if (sp.J1 <= sp.J0) continue;
+        // the previous unit's S MMAs have read its Q tiles
+        if (qc >= 1 && !(ok = mbar_wait_warp(&bars[Q_EMPTY], (qc - 1) & 1, wc, kErrWaitStageEmpty))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[Q_FULL], (sp.has[0] + sp.has[1]) * C::TILE);
+          for (int w = 0; w < 2; ++w) {
+            if (!sp.has[w]) continue;
+#pragma unroll
+            for (int s = 0; s < C::NSLAB; ++s)
+              tma_load_4d(sm + C::OFF_Q + w * C::TILE + s * C::SLAB, &maps.q, &bars[Q_FULL], s * 64, u.h,
+                          u.seq_start + u.q0 + w * BQ, u.b);
+          }
+        }
+        q_pend = qc & 1;
+        ++qc;
+        const int kvh = u.h / p.G;
+        for (int j = sp.J0; j < sp.J1; ++j, ++kc) {
+          const int st = kc % ST, n = kc / ST;
+          if (n >= 1 && !(ok = mbar_wait_warp(&bars[KV_EMPTY0 + st], (n - 1) & 1, wc, kErrWaitStageEmpty))) break;
+          uint8_t* dk = sm + C::OFF_KV + 2 * st * C::TILE;
+          uint8_t* dv = dk + C::TILE;
+          const int pos = u.seq_start + j * BK;
+          int r0, r1;
+          tail_rows(pos, BK, tail0, rows, &r0, &r1);
+          if (r0 < r1) {
+            // loaded onto the producer's own barrier, the tail rows zeroed, then published
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bars[TAIL], 2 * C::TILE);
+#pragma unroll
+              for (int s = 0; s < C::NSLAB; ++s) {
+                tma_load_4d(dk + s * C::SLAB, &maps.k, &bars[TAIL], s * 64, kvh, pos, u.b);
+                tma_load_4d(dv + s * C::SLAB, &maps.v, &bars[TAIL], s * 64, kvh, pos, u.b);
+              }
+            }
+            tail_pend = tail_ph & 1;
+            if (!(ok = mbar_wait_warp(&bars[TAIL], tail_ph & 1, wc, kErrWaitTail))) break;
+            tail_pend = -1;
+            ++tail_ph;
+            zero_tile_rows(dk, C::NSLAB, C::SLAB, r0, r1, lane);
+            zero_tile_rows(dv, C::NSLAB, C::SLAB, r0, r1, lane);
+            if (lane == 0) {
+              mbar_arrive(&bars[K_FULL0 + st]);
+              mbar_arrive(&bars[V_FULL0 + st]);
+            }
+          } else if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[K_FULL0 + st], C::TILE);
+#pragma unroll
+            for (int s = 0; s < C::NSLAB; ++s)
+              tma_load_4d(dk + s * C::SLAB, &maps.k, &bars[K_FULL0 + st], s * 64, kvh, pos, u.b);
+            mbar_arrive_expect_tx(&bars[V_FULL0 + st], C::TILE);
+#pragma unroll
+            for (int s = 0; s < C::NSLAB; ++s)
+              tma_load_4d(dv + s * C::SLAB, &maps.v, &bars[V_FULL0 + st], s * 64, kvh, pos, u.b);
+          }
+        }
       }
-      // loads still in flight land before the CTA exits: the last ST blocks'
+      // loads still in flight land before the CTA exits: the last Q and the last ST blocks'
       if (lane == 0) {
         if (q_pend >= 0) mbar_drain(&bars[Q_FULL], q_pend);
         if (tail_pend >= 0) mbar_drain(&bars[TAIL], tail_pend);
-        for (int i = imax(0, issued - ST); i < issued; ++i) {
+        for (uint32_t i = kc > static_cast<uint32_t>(ST) ? kc - ST : 0u; i < kc; ++i) {
           mbar_drain(&bars[K_FULL0 + i % ST], (i / ST) & 1);
           mbar_drain(&bars[V_FULL0 + i % ST], (i / ST) & 1);
         }
       }
       __syncwarp();
-    } else if (warp == 9 && J1 > J0) {
+    } else if (warp == 9) {
       // ============================================================ MMA issuer
       constexpr uint32_t IDESC_S = idesc_f16(BF16, 128, BK, false, false);
       constexpr uint32_t IDESC_PV = idesc_f16(BF16, 128, D, false, true);
@@ -314,61 +376,83 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
       const uint64_t q_kmaj = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t k_kmaj = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);
       const uint64_t v_mn = sdesc_sw128(sbase + C::OFF_KV + C::TILE, C::SLAB, 1024);
-      int npv[2] = {0, 0};
+      uint32_t qc = 0, kc = 0, npv0 = 0, npv1 = 0, oc0 = 0, oc1 = 0;
       bool ok = true;
-      auto in = [&](int w, int j) { return has[w] && u.lo[w] <= j && j < u.hi[w]; };
-      auto issue_s = [&](int w, int j) {
-        const uint64_t ko0 = sdesc_step(2 * ((j - J0) % ST) * C::TILE);
-        const uint64_t qo = sdesc_step(w * C::TILE);
+      for (uint32_t uc = 0; ok; ++uc) {
+        const FwdUnit u = next_unit(uc, &ok);
+        if (!ok || !u.valid) break;
+        const UnitSpan sp = unit_span(u);
+        if (sp.J1 <= sp.J0) continue;
+        const int J0 = sp.J0, J1 = sp.J1;
+        const uint32_t kc0 = kc;  // block counter at the unit's first block
+        auto in = [&](int w, int j) { return sp.has[w] && u.lo[w] <= j && j < u.hi[w]; };
+        auto issue_s = [&](int w, int j) {
+          const uint64_t ko0 = sdesc_step(2 * ((kc0 + j - J0) % ST) * C::TILE);
+          const uint64_t qo = sdesc_step(w * C::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ko = sdesc_step((kk / 4) * C::SLAB + (kk % 4) * 32);
-          mma_ss_w(tmem + (w ? C::T_S1 : C::T_S0), q_kmaj + qo + ko, k_kmaj + ko0 + ko, IDESC_S, kk > 0);
-        }
-        mma_commit_w(&bars[S_FULL0 + w]);
-      };
-      auto issue_pv = [&](int w, int j) -> bool {
-        if (!mbar_wait_warp(&bars[P_READY0 + w], npv[w] & 1, wc, kErrWaitP)) return false;
-        tc_fence_after();
-        const uint64_t vo = sdesc_step(2 * ((j - J0) % ST) * C::TILE);
-        const uint32_t ts = tmem + (w ? C::T_S1 : C::T_S0), to = tmem + (w ? C::T_O1 : C::T_O0);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_ts_w(to, ts + kk * 8, v_mn + vo + sdesc_step(kk * 2048), IDESC_PV, j > u.lo[w] || kk > 0);
-        mma_commit_w(&bars[O_DONE0 + w]);
-        ++npv[w];
-        return true;
-      };
-      auto wait_k = [&](int j) {
-        return mbar_wait_warp(&bars[K_FULL0 + (j - J0) % ST], ((j - J0) / ST) & 1, wc, kErrWaitKV);
-      };
-      ok = mbar_wait_warp(&bars[Q_FULL], 0, wc, kErrWaitStageFull) && wait_k(J0);
-      if (ok) {
-        tc_fence_after();
-        if (in(0, J0)) issue_s(0, J0);
-        if (in(1, J0)) issue_s(1, J0);
-      }
-      for (int j = J0; j < J1 && ok; ++j) {
-        const int st = (j - J0) % ST;
-        if (!(ok = mbar_wait_warp(&bars[V_FULL0 + st], ((j - J0) / ST) & 1, wc, kErrWaitKV))) break;
-        tc_fence_after();
-        if (in(0, j) && !(ok = issue_pv(0, j))) break;
-        const bool next = j + 1 < J1;
-        if (next) {
-          if (!(ok = wait_k(j + 1))) break;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ko = sdesc_step((kk / 4) * C::SLAB + (kk % 4) * 32);
+            mma_ss_w(tmem + (w ? C::T_S1 : C::T_S0), q_kmaj + qo + ko, k_kmaj + ko0 + ko, IDESC_S, kk > 0);
+          }
+          mma_commit_w(&bars[S_FULL0 + w]);
+        };
+        auto issue_pv = [&](int w, int j) -> bool {
+          uint32_t& npv = w ? npv1 : npv0;
+          if (!mbar_wait_warp(&bars[P_READY0 + w], npv & 1, wc, kErrWaitP)) return false;
+          if (j == u.lo[w]) {
+            // the tile's O accumulator: its softmax warps have read the previous unit's O
+            const uint32_t oc = w ? oc1 : oc0;
+            if (oc >= 1 && !mbar_wait_warp(&bars[O_FREE0 + w], (oc - 1) & 1, wc, kErrWaitDQEmpty)) return false;
+          }
           tc_fence_after();
-          if (in(0, j + 1)) issue_s(0, j + 1);
+          const uint64_t vo = sdesc_step(2 * ((kc0 + j - J0) % ST) * C::TILE);
+          const uint32_t ts = tmem + (w ? C::T_S1 : C::T_S0), to = tmem + (w ? C::T_O1 : C::T_O0);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_ts_w(to, ts + kk * 8, v_mn + vo + sdesc_step(kk * 2048), IDESC_PV, j > u.lo[w] || kk > 0);
+          mma_commit_w(&bars[O_DONE0 + w]);
+          ++npv;
+          return true;
+        };
+        auto wait_k = [&](int j) {
+          const uint32_t i = kc0 + j - J0;
+          return mbar_wait_warp(&bars[K_FULL0 + i % ST], (i / ST) & 1, wc, kErrWaitKV);
+        };
+        ok = mbar_wait_warp(&bars[Q_FULL], qc & 1, wc, kErrWaitStageFull) && wait_k(J0);
+        ++qc;
+        if (ok) {
+          tc_fence_after();
+          if (in(0, J0)) issue_s(0, J0);
+          if (in(1, J0)) issue_s(1, J0);
         }
-        if (in(1, j) && !(ok = issue_pv(1, j))) break;
-        mma_commit_w(&bars[KV_EMPTY0 + st]);  // every reader of K_j and V_j issued
-        if (next && in(1, j + 1)) issue_s(1, j + 1);
+        for (int j = J0; j < J1 && ok; ++j) {
+          const uint32_t i = kc0 + j - J0;
+          const int st = i % ST;
+          if (!(ok = mbar_wait_warp(&bars[V_FULL0 + st], (i / ST) & 1, wc, kErrWaitKV))) break;
+          tc_fence_after();
+          if (in(0, j) && !(ok = issue_pv(0, j))) break;
+          const bool next = j + 1 < J1;
+          if (next) {
+            if (!(ok = wait_k(j + 1))) break;
+            tc_fence_after();
+            if (in(0, j + 1)) issue_s(0, j + 1);
+          }
+          if (in(1, j) && !(ok = issue_pv(1, j))) break;
+          mma_commit_w(&bars[KV_EMPTY0 + st]);  // every reader of K_j and V_j issued
+          if (next && in(1, j + 1)) issue_s(1, j + 1);
+        }
+        if (!ok) break;
+        mma_commit_w(&bars[Q_EMPTY]);  // every S MMA of the unit issued
+        kc += J1 - J0;
+        oc0 += sp.has[0] ? 1u : 0u;
+        oc1 += sp.has[1] ? 1u : 0u;
       }
       // every MMA issued by this warp completes before TMEM is released
       mma_commit_w(&bars[DRAIN]);
       if (lane == 0) mbar_drain(&bars[DRAIN], 0);
       __syncwarp();
     }
-    // warps 10-11 (and 8-9 of a unit without keys): nothing to do
+    // warps 10-11: nothing to do
     finish();
     return;
   }
@@ -380,15 +464,19 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t tS = tmem + lane_off + (w ? C::T_S1 : C::T_S0);
   const uint32_t tO = tmem + lane_off + (w ? C::T_O1 : C::T_O0);
-  const int qt0 = u.q0 + w * BQ;  // first (sequence-local) query of the tile
-  const int lo_w = w ? u.lo[1] : u.lo[0], hi_w = w ? u.hi[1] : u.hi[0];
-  const int q = qt0 + row;
   const bool cm = p.causal || p.window > 0;
   const int W = p.window;
-  float m_used = -INFINITY, l = 0.f;
-  int c = 0;
+  uint32_t c = 0;  // blocks of this tile over all units so far
   bool ok = true;
-  if (qt0 < u.qlen && lo_w < hi_w) {
+  for (uint32_t uc = 0; ok; ++uc) {
+    const FwdUnit u = next_unit(uc, &ok);
+    if (!ok || !u.valid) break;
+    const int qt0 = u.q0 + w * BQ;  // first (sequence-local) query of the tile
+    if (qt0 >= u.qlen) continue;    // the tile is past the end of its sequence
+    const int lo_w = w ? u.lo[1] : u.lo[0], hi_w = w ? u.hi[1] : u.hi[0];
+    const int q = qt0 + row;
+    const uint32_t c0 = c;
+    float m_used = -INFINITY, l = 0.f;
     for (int j = lo_w; j < hi_w; ++j, ++c) {
       if (!(ok = mbar_wait_warp(&bars[S_FULL0 + w], c & 1, wc, kErrWaitS))) break;
       tc_fence_after();
@@ -405,13 +493,16 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int k = 0; k < BK; ++k) mx = fmaxf(mx, __uint_as_float(sr[k]));
       } else {
+        // keys k in [k_lo, k_hi) of the block are visible to my query (one range per row)
+        const int64_t d0 = static_cast<int64_t>(q) + u.off - k0;  // my key position relative to the block
+        int64_t lo = 0, hi = u.klen - k0;
+        if (cm) hi = hi < d0 + 1 ? hi : d0 + 1;
+        if (W > 0) lo = d0 - W + 1 > 0 ? d0 - W + 1 : 0;
+        if (q >= u.qlen) hi = 0;
+        const int k_lo = static_cast<int>(lo > BK ? BK : lo), k_hi = static_cast<int>(hi < 0 ? 0 : (hi > BK ? BK : hi));
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-          const int kpos = k0 + k;
-          bool vis = kpos < u.klen && q < u.qlen;
-          if (cm) vis = vis && kpos <= q + u.off;
-          if (W > 0) vis = vis && q + u.off < kpos + W;
-          const float s = vis ? __uint_as_float(sr[k]) : -INFINITY;
+          const float s = (k >= k_lo && k < k_hi) ? __uint_as_float(sr[k]) : -INFINITY;
           sr[k] = __float_as_uint(s);
           mx = fmaxf(mx, s);
         }
@@ -423,7 +514,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
       const bool resc = m_used != -INFINITY && m_new > m_used + kRescaleLog2;
       const float f = resc ? ex2(m_used - m_new) : 1.f;
       if (__any_sync(0xffffffffu, resc)) {
-        // the tile's previous P V has completed before its O rows are scaled
+        // the tile's previous P V (of this unit: m_used is finite) has completed
+        // before its O rows are scaled
         if (!(ok = mbar_wait_warp(&bars[O_DONE0 + w], (c - 1) & 1, wc, kErrWaitDQFull))) break;
         tc_fence_after();
 #pragma unroll 1
@@ -461,14 +553,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[P_READY0 + w]);
     }
-  }
-  if (ok && qt0 < u.qlen) {
+    if (!ok) break;
     // ---- O = O_w / l and the natural-log LSE of the row
-    if (c > 0) {
-      if (!(ok = mbar_wait_warp(&bars[O_DONE0 + w], (c - 1) & 1, wc, kErrWaitDQFull))) {
-        finish();
-        return;
-      }
+    const bool had = c > c0;  // the tile saw a key block in this unit
+    if (had) {
+      if (!(ok = mbar_wait_warp(&bars[O_DONE0 + w], (c - 1) & 1, wc, kErrWaitDQFull))) break;
       tc_fence_after();
     }
     const bool live = q < u.qlen;
@@ -481,7 +570,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t r[32];
-      if (c > 0) {
+      if (had) {
         tmem_ld32(tO + ch * 32, r);
         tmem_ld_wait();
       } else {
@@ -499,6 +588,12 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
           *reinterpret_cast<uint4*>(out + 2 * (ch * 32 + c8 * 8)) = v;
         }
       }
+    }
+    if (had) {
+      // this unit's O rows are read: the next unit's first P V may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[O_FREE0 + w]);
     }
   }
   finish();

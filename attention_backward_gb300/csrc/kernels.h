@@ -74,6 +74,7 @@ struct FwdParams {
   float* lse;  // f32, lse[b*sl_b + h*sl_h + s*sl_s]
   int64_t sl_b, sl_s, sl_h;
   int* err;
+  int* unit_counter;  // cleared before the launch; persistent CTAs draw units from it
   uint64_t timeout_ns;
 };
 

@@ -172,7 +172,8 @@ ATTN_BWD_API attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const 
  * under the mask, and the natural-log LSE of every query row (the TileOPs
  * page's backward op takes q, k, v, o, do, lse, "Summary"; the rows computed
  * are the first half of its "Reference" program: masked scores, their softmax
- * and log-sum-exp).  One CTA per two 128-row query tiles of one query head;
+ * and log-sum-exp).  Persistent CTAs, one per SM, walk units of two 128-row
+ * query tiles of one query head;
  * tcgen05 MMAs with the scores and O in tensor memory, the row max updated
  * lazily (O rescaled only when a row max grows by more than 2^8).
  *   q, o : [B,S,HQ,D] 16-bit;  k, v : [B,Sk,HKV,D] 16-bit (Sk as for
