@@ -620,16 +620,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (gs >= 1 && !(ok = mbar_wait_warp(&bars[DS_SFREE], (gs - 1) & 1, wc, kErrWaitDSFree))) break;
         tc_fence_after();
         uint8_t* dsb = sm + OFF_DS + wg * DS_BLOCK;
-        // bf16: the step takes the rounding residuals if any softmax warp saw a
-        // large P (P_READY completes once all eight have flagged or not; the flag
-        // of step gs is rewritten only at step gs + 2)
-        bool split = big;
-        if constexpr (SPLIT) {
-          if (!split) {
-            if (!(ok = mbar_wait_warp(&bars[P_READY], gs & 1, wc, kErrWaitP))) break;
-            split = split_flag[gs & 1] == gs + 1;
-          }
-        }
+        // the step takes the rounding residuals if any softmax warp saw a large P
+        // (the MMA warp reads the flag after every warp has signalled); a warp
+        // with a large P writes its residual pairs, the others write zeros there
+        const bool split = big;
         // dS for 16 queries at a time: dS^T pairs into the second half of this
         // warpgroup's S^T columns and dS as the MN-major A operand of dQ (64-query
         // block wg, row = key, two 16-byte chunks).  A step with the residuals
@@ -638,15 +632,24 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         // pairs; read by the residual MMAs, then overwritten by this step's dQ),
         // and loads the second half of its dP^T columns only when it reaches
         // them, which keeps the residuals within the warp's registers.
-        auto ds_stage = [&](auto split_c) {
-          constexpr bool SPLIT = decltype(split_c)::value;
+        auto ds_stage = [&](auto res_c) {
+          constexpr bool RES = decltype(res_c)::value;
           uint32_t dr[HALF];
           tmem_ld32(tmem + lane_off + T_DP + wg * HALF, dr);
-          if constexpr (!SPLIT) tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
+          if constexpr (!RES) tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
           tmem_ld_wait();
+          if constexpr (SPLIT && !RES) {
+            // a warp without large P: zero residual pairs, in case another warp of
+            // the step flagged it and the residual MMAs read these columns
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+            for (int c16 = 0; c16 < HALF / 16; ++c16) tmem_st16(tmem + lane_off + T_DP + wg * HALF + 16 * c16, z);
+          }
 #pragma unroll
           for (int g = 0; g < HALF / 16; ++g) {
-            if constexpr (SPLIT) {
+            if constexpr (RES) {
               if (g == HALF / 32) {
                 tmem_ld32(tmem + lane_off + T_DP + wg * HALF + 32, dr + 32);
                 tmem_ld_wait();
@@ -663,7 +666,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
               const float d3 = pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w);
               dsw[c / 2] = pack2<BF16>(d0, d1);
               dsw[c / 2 + 1] = pack2<BF16>(d2, d3);
-              if constexpr (SPLIT) {
+              if constexpr (RES) {
                 dsl[c / 2] = lo_pair<BF16>(d0, d1, dsw[c / 2]);
                 dsl[c / 2 + 1] = lo_pair<BF16>(d2, d3, dsw[c / 2 + 1]);
                 plo[c / 2] = lo_pair<BF16>(pv[cc], pv[cc + 1], pack2<BF16>(pv[cc], pv[cc + 1]));
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
             for (int c4 = 0; c4 < 2; ++c4)
               *reinterpret_cast<uint4*>(dsb + sw128_offset(row, g * 2 + c4)) =
                   make_uint4(dsw[c4 * 4], dsw[c4 * 4 + 1], dsw[c4 * 4 + 2], dsw[c4 * 4 + 3]);
-            if constexpr (SPLIT) {
+            if constexpr (RES) {
               const uint32_t lo_col = tmem + lane_off + T_DP + wg * HALF + g * 16;
               tmem_st8(lo_col, plo);
               tmem_st8(lo_col + 8, dsl);

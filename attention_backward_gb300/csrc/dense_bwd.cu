@@ -645,16 +645,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             !(ok = mbar_wait_warp(&bars[DS_SFREE0 + gs % C::NDS], ((gs - C::NDS) / C::NDS) & 1, wc, kErrWaitDSFree)))
           break;
         tc_fence_after();
-        // bf16: the step takes the rounding residuals if any softmax warp saw a
-        // large P (its P_READY completes once all eight have flagged or not; the
-        // flag of step gs is rewritten only at step gs + 2)
-        bool split = big;
-        if constexpr (SPLIT) {
-          if (!split) {
-            if (!(ok = mbar_wait_warp(&bars[P_READY0 + (gs & 1)], (gs >> 1) & 1, wc, kErrWaitP))) break;
-            split = split_flag[gs & 1] == gs + 1;
-          }
-        }
+        // the step takes the rounding residuals if any softmax warp saw a large P
+        // (the MMA warp reads the flag after every warp has signalled); a warp
+        // with a large P writes its residual pairs, the others write zeros there
+        const bool split = big;
         uint8_t* const dsbase = sm + C::OFF_DS + (gs % C::NDS) * C::DS_BYTES + wg * (BM * 128);
         // dS for 16 queries at a time: dS^T pairs into the second half of this
         // warpgroup's S^T columns, dS as the MN-major A operand of dQ (64-query
@@ -665,18 +659,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
         // pairs; the next dP^T is issued after the residual MMAs) and loads the
         // second half only when it reaches it, keeping the residuals within the
         // warp's registers.
-        auto ds_stage = [&](auto split_c) {
-          constexpr bool SPLIT = decltype(split_c)::value;
+        auto ds_stage = [&](auto res_c) {
+          constexpr bool RES = decltype(res_c)::value;
           uint32_t dr[HALF];
           tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF, dr);
-          if constexpr (!SPLIT) tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + 32, dr + 32);
+          if constexpr (!RES) tmem_ld32(tmem + lane_off + C::T_DP + wg * HALF + 32, dr + 32);
           tmem_ld_wait();
           auto dp_loaded = [&]() {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[DP_FREE]);
           };
-          if constexpr (!SPLIT) {
+          if constexpr (!RES) {
+            if constexpr (SPLIT) {
+              // a warp without large P: zero residual pairs, in case another warp
+              // of the step flagged it and the residual MMAs read these columns
+              // (complete before the next step's dP^T may overwrite them)
+              uint32_t z[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+              for (int c16 = 0; c16 < HALF / 16; ++c16)
+                tmem_st16(tmem + lane_off + C::T_DP + wg * HALF + 16 * c16, z);
+              tmem_st_wait();
+            }
             dp_loaded();
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
