@@ -192,6 +192,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the preprocess (the previous kernel on the stream) has written LSE2, delta,
+  // the cleared accumulators and tile counter; the landing may be scheduled now
+  grid_dependency_wait();
+  grid_dependents_launch();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
   // Every role ends here: all warps meet, then the MMA warp releases TMEM.
@@ -806,8 +810,8 @@ cudaError_t launch_t(const DenseParams& p, const DenseMaps& m, int grid, cudaStr
   auto kern = dense128_bwd_kernel<BF16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, SMEM, st>>>(m, p);
-  return cudaGetLastError();
+  e = launch_after_previous(kern, grid, THREADS, SMEM, st, m, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -196,6 +196,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the preprocess (the previous kernel on the stream) has written LSE2, delta,
+  // the cleared accumulators and tile counter; the landing may be scheduled now
+  grid_dependency_wait();
+  grid_dependents_launch();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
   // Every role ends here: all warps meet, then the MMA warp releases TMEM.
@@ -848,8 +852,8 @@ cudaError_t launch_dense_t(const DenseParams& p, const DenseMaps& m, int grid, c
   auto kern = dense_bwd_kernel<D, BF16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM, st>>>(m, p);
-  return cudaGetLastError();
+  e = launch_after_previous(kern, grid, Cfg<D>::THREADS, Cfg<D>::SMEM, st, m, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // One CTA waits on a barrier that nothing signals: the bounded wait must give

@@ -125,6 +125,25 @@ attn_status_t check_gqa_call(const void* q, attn_strides_t sq, const void* k, at
                              attn_strides_t sdq, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
                              void* workspace, size_t workspace_bytes);
 
+// Launches ``kern`` with programmatic stream serialization: it may be scheduled
+// while the previous kernel on ``st`` finishes, and waits for it with
+// grid_dependency_wait before reading its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_previous(void (*kern)(KArgs...), int grid, int threads, int smem, cudaStream_t st,
+                                  Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Block sizes of both dense kernels: keys per tile, and queries per step
 // (every MMA at N = 128; 64-query steps with a double-buffered S^T measured
 // slower at head dim 128 on both the causal and the unmasked workloads).

@@ -156,6 +156,10 @@ __global__ void __maxnreg__(168)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the preprocess (the previous kernel on the stream) has written LSE2, delta,
+  // the cleared accumulators and tile counter; the landing may be scheduled now
+  grid_dependency_wait();
+  grid_dependents_launch();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int units_total = p.B * p.S * p.HKV;
 
@@ -527,8 +531,8 @@ cudaError_t launch_t(const SparseParams& p, const SparseMaps& m, int grid, cudaS
   auto kern = sparse_bwd_kernel<BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, SMEM, st>>>(m, p);
-  return cudaGetLastError();
+  e = launch_after_previous(kern, grid, THREADS, SMEM, st, m, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
