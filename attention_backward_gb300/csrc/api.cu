@@ -263,6 +263,7 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
   p.bn = BN;
   s->bf16 = dtype == ATTN_DT_BF16;
   s->grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  p.tile_group = tile_group(s->grid, static_cast<int>((Sk + kDenseBM - 1) / kDenseBM));
   return ATTN_OK;
 }
 
@@ -518,6 +519,7 @@ void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_
   if (B >= 1 && S >= 1 && HKV >= 1 && (!cu_seqlens || num_seqs >= 1)) {
     DenseParams p{};
     p.B = B, p.S = S, p.Sk = S, p.HKV = HKV;
+    p.tile_group = kTileGroup;
     p.causal = causal ? 1 : 0, p.window = window_left;
     p.cu_seqlens = cu_seqlens, p.num_seqs = cu_seqlens ? num_seqs : 0;
     p.bn = kDenseBN;

@@ -39,15 +39,24 @@ constexpr uint32_t kSplitPBf16x2 = 0x3E003E00u;  // kSplitP as two bf16 patterns
 // run without the check (it costs the softmax warps a few percent).
 constexpr int kSplitMinGroup = 4;
 
-// (batch, KV head) pairs whose tiles are drawn together (dense batches).
+// (batch, KV head) pairs whose tiles are drawn together (dense batches): at
+// most kTileGroup, and no more than the CTAs in flight can cover at once
+// (about one tile of every pair of the group per CTA).
 constexpr int kTileGroup = 8;
+__host__ __device__ inline int tile_group(int ctas, int tiles_per_pair) {
+  const int g = tiles_per_pair > 0 ? ctas / tiles_per_pair : kTileGroup;
+  return g < 1 ? 1 : (g > kTileGroup ? kTileGroup : g);
+}
 
 // Tile t -> (batch, KV head, key block); longest tiles first (smallest key
 // block index first, which is the longest under a causal mask).  Dense
-// batches go through the (batch, KV head) pairs in groups of kTileGroup,
+// batches go through the (batch, KV head) pairs in groups of p.tile_group,
 // key block major inside a group: the CTAs in flight then share the Q/dO rows
 // and dQ accumulator rows of a few heads, which stay in L2, at no cost in
-// load balance (each group still ends with its shortest tiles).  Packed
+// load balance (each group still ends with its shortest tiles).  Long rows
+// (more key tiles per pair than CTAs) take groups of one pair: all CTAs then
+// work on the same KV head, whose dQ accumulator rows fit L2, instead of
+// sweeping the accumulators of several heads at once.  Packed
 // sequences keep key block major order over all pairs (their tile count per
 // pair is known only on the device, and the draws past it end a CTA's work).
 // Host code may call it too (with cu_seqlens in host memory) to check the order.
@@ -59,7 +68,7 @@ static __host__ __device__ __forceinline__ TileInfo decode_tile(int t, const Den
   int bh, r;
   if (p.cu_seqlens == nullptr) {
     const int nt = (p.Sk + kDenseBM - 1) / kDenseBM;  // key tiles per pair
-    const int grp = imin(BH, kTileGroup);
+    const int grp = imin(BH, p.tile_group > 0 ? p.tile_group : kTileGroup);
     const int gi = t / (grp * nt);
     const int g0 = gi * grp;
     if (g0 >= BH) return ti;

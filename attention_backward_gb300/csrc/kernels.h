@@ -55,6 +55,7 @@ struct DenseParams {
   uint64_t timeout_ns;
   int* tile_counter;  // zeroed by the preprocess; persistent CTAs draw tiles from it
   int bn;             // query rows per step (the tile schedule's query block)
+  int tile_group;     // (batch, KV head) pairs drawn together, dense batches (tile_group())
 };
 
 struct DenseMaps {

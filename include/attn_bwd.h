@@ -306,7 +306,9 @@ ATTN_BWD_API void attn_bwd_query_block_range_qk(int32_t k0, int32_t block_k, int
  * keys, query blocks 128 rows; dense batches go through the (batch, KV head)
  * pairs in groups of 8, key block major inside a group (the longest tiles of a
  * group first under a causal mask), packed sequences key block major over all
- * pairs.  Writes out[0..6] = {valid, b, kv head, sequence start, first key
+ * pairs.  (A launch sizes its groups by the CTAs in flight: rows with more key
+ * tiles per pair than CTAs take groups of one pair; this helper shows the
+ * groups of 8.)  Writes out[0..6] = {valid, b, kv head, sequence start, first key
  * (sequence-local), first query block, number of query blocks}; valid = 0 for
  * a draw past the last tile or invalid sizes (B, S, HKV < 1). */
 ATTN_BWD_API void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t causal,
