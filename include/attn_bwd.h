@@ -363,7 +363,7 @@ ATTN_BWD_API attn_status_t attn_bwd_gqa_noalloc(const void* q, attn_strides_t sq
 ATTN_BWD_API attn_status_t attn_bwd_noalloc_check_error(void* stream, int32_t* device_code);
 
 /* Device scratch bytes that attn_bwd_gqa_host needs to process the problem
- * in ``chunks`` chunks of KV heads (0 for an invalid shape). */
+ * in about ``chunks`` chunks (0 for an invalid shape). */
 ATTN_BWD_API size_t attn_bwd_host_scratch_size(int64_t B, int64_t S, int64_t HQ, int64_t HKV, int64_t D,
                                                int64_t chunks);
 
@@ -371,10 +371,12 @@ ATTN_BWD_API size_t attn_bwd_host_scratch_size(int64_t B, int64_t S, int64_t HQ,
  * host<->device copies overlapped with the kernels.  This entry point is a
  * convenience of this library; the pages it follows have no counterpart.
  *
- * The problem is split into ceil(HKV / ceil(HKV / chunks)) chunks of KV heads;
- * a chunk and its query heads are independent of the others.  Each chunk is
- * copied in (strided head slices of the host tensors into contiguous device
- * buffers, on ``copy_in_stream``), run through attn_bwd_gqa (its three
+ * The problem is split into chunks of batch rows and KV heads; a chunk (its
+ * KV heads and their query heads) is independent of the others.  With
+ * chunks >= B each batch row is split into ceil(HKV / ceil(HKV / (chunks / B)))
+ * ranges of KV heads; with chunks < B a chunk is ceil(B / chunks) whole batch
+ * rows.  Each chunk is copied in (strided slices of the host tensors into
+ * contiguous device buffers, on ``copy_in_stream``), run through attn_bwd_gqa (its three
  * launches, on ``stream``) and copied out (on
  * ``copy_out_stream``), with two buffer slots so that copies of neighbouring
  * chunks overlap the kernels.  The copies start after the work queued on

@@ -1,5 +1,6 @@
 """attn_bwd_gqa_host: the dense backward from host buffers to host buffers,
-chunk by chunk of KV heads with the copies overlapped with the kernels.  Every
+chunk by chunk of batch rows and KV heads with the copies overlapped with the
+kernels.  Every
 chunk runs the same kernels on the same tiles as a single call, so dK and dV
 (written once per tile) must be bit-identical to the device path; dQ (summed
 from key tiles in a scheduling-dependent order) is checked against the oracle.
@@ -24,6 +25,9 @@ CASES = [
     (inputs.scaled(C3, name="gqa_g4_causal_b2_f16", B=2, S=300, HQ=16, HKV=4, causal=True, dtype="f16"), 4),
     # more chunks than KV heads: one KV head per chunk
     (inputs.scaled(C4, name="varlen_window_d64", S=900, HQ=4, HKV=2, window=200, cu_seqlens=(0, 333, 900)), 8),
+    # batch rows split first: 3 rows x 2 ranges of KV heads; and fewer chunks than rows (2 rows per chunk)
+    (inputs.scaled(C3, name="gqa_b3_causal_f16", B=3, S=260, HQ=8, HKV=4, causal=True, dtype="f16"), 6),
+    (inputs.scaled(C3, name="gqa_b3_rows_per_chunk_bf16", B=3, S=200, HQ=4, HKV=2), 2),
 ]
 
 
