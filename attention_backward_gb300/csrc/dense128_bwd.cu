@@ -386,10 +386,12 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         }
         // LSE2/delta of the stage were last read by the softmax of step gs - ST,
         // which finished before that step's dQ (and so before EMPTY0)
+        // negated, so that the softmax forms S*scale - LSE2 and dP - delta
+        // with paired f32 adds and fused multiply-adds
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
-          s_lse[st * BN + lane + 32 * i] = nl[i];
-          s_delta[st * BN + lane + 32 * i] = nd[i];
+          s_lse[st * BN + lane + 32 * i] = -nl[i];
+          s_delta[st * BN + lane + 32 * i] = -nd[i];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[FULL0 + st]);
@@ -564,14 +566,21 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         tmem_ld32(sb + wg * HALF, sr);
         tmem_ld32(sb + wg * HALF + 32, sr + 32);
         tmem_ld_wait();
+        // S^T * scale - LSE2 two columns per instruction (f32x2 FMA)
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        auto x_pair = [&](int cc, float lo, float hi) {
+          return __ffma2_rn(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2,
+                            make_float2(lo, hi));
+        };
         if (full_vis) {
 #pragma unroll
           for (int c4 = 0; c4 < HALF / 4; ++c4) {
-            const float4 t = lse4[c4];
-            const float l4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pv[4 * c4 + e] = ex2(fmaf(__uint_as_float(sr[4 * c4 + e]), p.scale_log2, -l4[e]));
+            const float4 t = lse4[c4];  // -LSE2
+            const float2 x0 = x_pair(4 * c4, t.x, t.y), x1 = x_pair(4 * c4 + 2, t.z, t.w);
+            pv[4 * c4] = ex2(x0.x);
+            pv[4 * c4 + 1] = ex2(x0.y);
+            pv[4 * c4 + 2] = ex2(x1.x);
+            pv[4 * c4 + 3] = ex2(x1.y);
           }
         } else {
           // my columns cc in [c_lo, c_hi) are visible: a real query (cc < qlen -
@@ -583,13 +592,14 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
           const int c_hi = imin(ti.qlen - qc0, static_cast<int>(hi < 0 ? 0 : (hi > HALF ? HALF : hi)));
 #pragma unroll
           for (int c4 = 0; c4 < HALF / 4; ++c4) {
-            const float4 t = lse4[c4];
-            const float l4[4] = {t.x, t.y, t.z, t.w};
+            const float4 t = lse4[c4];  // -LSE2
+            const float2 x0 = x_pair(4 * c4, t.x, t.y), x1 = x_pair(4 * c4 + 2, t.z, t.w);
+            const float x4[4] = {x0.x, x0.y, x1.x, x1.y};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int cc = 4 * c4 + e;
               const bool vis = kvalid && cc >= c_lo && cc < c_hi;
-              pv[cc] = vis ? ex2(fmaf(__uint_as_float(sr[cc]), p.scale_log2, -l4[e])) : 0.f;
+              pv[cc] = vis ? ex2(x4[e]) : 0.f;
             }
           }
         }
@@ -663,11 +673,15 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
 #pragma unroll
             for (int c = 0; c < 16; c += 4) {
               const int cc = g * 16 + c;
-              const float4 dl = dlt4[cc / 4];  // delta of columns cc .. cc + 3
-              const float d0 = pv[cc] * (__uint_as_float(dr[cc]) - dl.x);
-              const float d1 = pv[cc + 1] * (__uint_as_float(dr[cc + 1]) - dl.y);
-              const float d2 = pv[cc + 2] * (__uint_as_float(dr[cc + 2]) - dl.z);
-              const float d3 = pv[cc + 3] * (__uint_as_float(dr[cc + 3]) - dl.w);
+              const float4 dl = dlt4[cc / 4];  // -delta of columns cc .. cc + 3
+              // dS = P (dP - delta), two columns per instruction (f32x2 add and multiply)
+              const float2 a0 = __fmul2_rn(make_float2(pv[cc], pv[cc + 1]),
+                                           __fadd2_rn(make_float2(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])),
+                                                      make_float2(dl.x, dl.y)));
+              const float2 a1 = __fmul2_rn(make_float2(pv[cc + 2], pv[cc + 3]),
+                                           __fadd2_rn(make_float2(__uint_as_float(dr[cc + 2]), __uint_as_float(dr[cc + 3])),
+                                                      make_float2(dl.z, dl.w)));
+              const float d0 = a0.x, d1 = a0.y, d2 = a1.x, d3 = a1.y;
               dsw[c / 2] = pack2<BF16>(d0, d1);
               dsw[c / 2 + 1] = pack2<BF16>(d2, d3);
               if constexpr (RES) {

@@ -488,10 +488,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
       // every key and query of the block in range and inside the mask
       const bool full_vis = k0 + BK <= u.klen && qt0 + BQ <= u.qlen && (!cm || qt0 + u.off >= k0 + BK - 1) &&
                             (W <= 0 || qt0 + BQ - 1 + u.off < k0 + W);
-      float mx = -INFINITY;
+      // row max over four independent chains
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full_vis) {
 #pragma unroll
-        for (int k = 0; k < BK; ++k) mx = fmaxf(mx, __uint_as_float(sr[k]));
+        for (int k = 0; k < BK; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[k]));
       } else {
         // keys k in [k_lo, k_hi) of the block are visible to my query (one range per row)
         const int64_t d0 = static_cast<int64_t>(q) + u.off - k0;  // my key position relative to the block
@@ -504,9 +505,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
         for (int k = 0; k < BK; ++k) {
           const float s = (k >= k_lo && k < k_hi) ? __uint_as_float(sr[k]) : -INFINITY;
           sr[k] = __float_as_uint(s);
-          mx = fmaxf(mx, s);
+          mx4[k & 3] = fmaxf(mx4[k & 3], s);
         }
       }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       // the row max in log2 units (scale_log2 > 0 keeps the order of the raw scores)
       const float m_new = fmaxf(m_used, mx * p.scale_log2);
       // a row whose max grew past the threshold is rescaled; a row that had no
@@ -532,22 +534,26 @@ __global__ void __launch_bounds__(THREADS, 1) dense_fwd_kernel(const __grid_cons
       l *= f;
       if (resc || m_used == -INFINITY) m_used = m_new;
       const float msub = m_used == -INFINITY ? 0.f : m_used;
-      float sum = 0.f;
+      // S * scale - m two keys per instruction (f32x2 FMA), the row sum in two
+      // f32x2 accumulators
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-msub, -msub);
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int ch = 0; ch < BK / 32; ++ch) {
         uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[ch * 32 + 2 * e]), p.scale_log2, -msub));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[ch * 32 + 2 * e + 1]), p.scale_log2, -msub));
-          sum += p0 + p1;
-          pw[e] = pack2<BF16>(p0, p1);
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sr[ch * 32 + 2 * e]), __uint_as_float(sr[ch * 32 + 2 * e + 1])), sc2, nm2);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          sum2[e & 1] = __fadd2_rn(sum2[e & 1], pp);
+          pw[e] = pack2<BF16>(pp.x, pp.y);
         }
         // P pairs of keys 32ch .. 32ch + 31 into S columns 16ch .. 16ch + 15 (the
         // scores of this row were all loaded above)
         tmem_st16(tS + ch * 16, pw);
       }
-      l += sum;
+      l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
