@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     dq_land,
     forward,
     gqa_main,
+    gqa_workspace_size,
     host_scratch_size,
     library,
     preprocess,
@@ -27,6 +28,8 @@ from ._binding import (  # noqa: F401
     sparse_backward,
     sparse_land,
     sparse_main,
+    tail_plan,
     tile_schedule,
+    tile_schedule_split,
     workspace_size,
 )

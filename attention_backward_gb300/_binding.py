@@ -35,6 +35,10 @@ class Mask(ctypes.Structure):
 
 _SIGS = {
     "attn_bwd_workspace_size": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
+    "attn_bwd_gqa_workspace_size": (c_sz, [c_i64, c_i64, c_i64, c_i64]),
+    "attn_bwd_tail_plan": (None, [c_i64, c_i32, c_i32, ctypes.POINTER(c_i32)]),
+    "attn_bwd_tile_schedule_split": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                            ctypes.POINTER(c_i32)]),
     "attn_bwd_preprocess": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_i64, c_i64, c_i64, c_i64, c_i64,
                                     c_i64, c_i32, c_vp, c_sz, c_vp]),
     "attn_bwd_gqa": (c_i32, [c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp, Strides, c_vp,
@@ -151,6 +155,31 @@ def workspace_size(B: int, S: int, H: int, Dq: int, dkv_elems: int = 0) -> int:
 def new_workspace(B: int, S: int, H: int, Dq: int, dkv_elems: int = 0, device=None) -> torch.Tensor:
     n = workspace_size(B, S, H, Dq, dkv_elems)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gqa_workspace_size(B: int, S: int, HQ: int, D: int) -> int:
+    """Workspace bytes with room for the one-call dense path's last-round split."""
+    return int(library().attn_bwd_gqa_workspace_size(B, S, HQ, D))
+
+
+def new_gqa_workspace(B: int, S: int, HQ: int, D: int, device=None) -> torch.Tensor:
+    return torch.empty(gqa_workspace_size(B, S, HQ, D), dtype=torch.uint8, device=device or "cuda")
+
+
+def tail_plan(tiles: int, ctas: int, G: int) -> tuple:
+    """(first split draw, split tiles, query heads per unit); zeros: no split."""
+    out = (c_i32 * 3)()
+    library().attn_bwd_tail_plan(tiles, ctas, G, out)
+    return tuple(out)
+
+
+def tile_schedule_split(t: int, B: int, S: int, HKV: int, G: int, tail_start: int, tail_tiles: int,
+                        tail_hpu: int) -> tuple:
+    """Draw t of an unmasked dense batch with a last-round split: the seven
+    values of tile_schedule, then (first head, heads, partials slot)."""
+    out = (c_i32 * 10)()
+    library().attn_bwd_tile_schedule_split(t, B, S, HKV, G, tail_start, tail_tiles, tail_hpu, out)
+    return tuple(out)
 
 
 def preprocess(o, do, lse, workspace, Dq: Optional[int] = None, dkv_elems: int = 0, stream=None) -> None:
@@ -349,7 +378,7 @@ def backward(q, k, v, o, do, lse, sm_scale: Optional[float] = None, causal: bool
     if sm_scale is None:
         sm_scale = D ** -0.5
     if workspace is None:
-        workspace = new_workspace(B, S, HQ, D, device=q.device)
+        workspace = new_gqa_workspace(B, S, HQ, D, device=q.device)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)

@@ -203,6 +203,7 @@ struct DenseSetup {
   DenseMaps m;
   bool bf16;
   int grid;
+  size_t part_bytes;  // last-round partials cleared before the launch (0: no split)
 };
 
 attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const void* k, attn_strides_t sk,
@@ -210,6 +211,7 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
                           int64_t HQ, int64_t HKV, int64_t D, attn_dtype_t dtype, float sm_scale,
                           const attn_mask_t* mask, void* dk, attn_strides_t sdk, void* dv, attn_strides_t sdv,
                           void* workspace, size_t workspace_bytes, bool encode = true) {
+  s->part_bytes = 0;
   if (!q || !k || !v || !dO || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || HQ < 1 || HKV < 1 || HQ % HKV != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return ATTN_ERR_INVALID_ARG;
@@ -267,7 +269,65 @@ attn_status_t setup_dense(DenseSetup* s, const void* q, attn_strides_t sq, const
   return ATTN_OK;
 }
 
+// The last-round split of a dense batch's key tiles: with T equal tiles on
+// ``ctas`` persistent CTAs the last round holds T mod ctas tiles, and the
+// other CTAs idle meanwhile.  Drawing those tiles as units of ``hpu`` query
+// heads (dK/dV partials added in f32) spreads them over all CTAs.  The
+// makespan is counted in 1/G tiles; the split is taken when it shortens the
+// last round by at least a quarter of a tile (half a tile at G = 2), with the
+// largest head count among equal makespans.
+struct TailPlan {
+  int start, tiles, hpu;  // tiles = 0: no split
+};
+TailPlan tail_plan(int64_t T, int64_t ctas, int G) {
+  TailPlan t{0, 0, 0};
+  if (G < 2 || ctas < 1 || T <= ctas) return t;
+  const int64_t full = T / ctas, R = T % ctas;
+  if (R == 0 || R > kMaxTailTiles) return t;
+  const int64_t whole = (full + 1) * G;
+  int64_t best = whole;
+  int hpu_best = 0;
+  for (int hpu = G - 1; hpu >= 1; --hpu) {
+    if (G % hpu) continue;
+    const int64_t units = R * (G / hpu);
+    const int64_t ms = full * G + (units + ctas - 1) / ctas * hpu;
+    if (ms < best) best = ms, hpu_best = hpu;
+  }
+  if (hpu_best == 0 || whole - best < (G / 4 > 1 ? G / 4 : 1)) return t;
+  t.start = static_cast<int>(T - R), t.tiles = static_cast<int>(R), t.hpu = hpu_best;
+  return t;
+}
+
+// f32 elements of the partials region for ``tiles`` split tiles at head dim D:
+// the per-quarter unit counters (padded to 256 bytes), then the partials.
+int64_t tail_region_elems(int64_t tiles, int64_t D) { return round_up(tiles * 4, 64) + tiles * 2 * D * kDenseBM; }
+
+// Enables the last-round split of a checked dense set-up when it applies (head
+// dim 128, an unmasked dense batch, more than one query head per KV head) and
+// the workspace has room for the partials behind the dQ accumulator; run_dense
+// then clears them before the launch.
+void plan_tail_split(DenseSetup* s, void* workspace, size_t workspace_bytes) {
+  DenseParams& p = s->p;
+  p.tail_start = p.tail_tiles = p.tail_hpu = 0;
+  s->part_bytes = 0;
+  if (p.D != 128 || p.cu_seqlens != nullptr || p.causal || p.window > 0) return;
+  const int64_t T = static_cast<int64_t>((p.Sk + kDenseBM - 1) / kDenseBM) * p.B * p.HKV;
+  const TailPlan t = tail_plan(T, s->grid, p.G);
+  if (t.tiles == 0) return;
+  const int64_t elems = tail_region_elems(t.tiles, p.D);
+  const WsLayout L = ws_layout(p.B, p.S, p.HQ, p.D, elems);
+  if (workspace_bytes < static_cast<size_t>(L.total)) return;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.tail_start = t.start, p.tail_tiles = t.tiles, p.tail_hpu = t.hpu;
+  p.part_count = reinterpret_cast<int*>(ws + L.dkv_off);
+  p.part_acc = reinterpret_cast<float*>(ws + L.dkv_off + round_up(t.tiles * 4, 64) * 4);
+  s->part_bytes = static_cast<size_t>(elems) * 4;
+}
+
 attn_status_t run_dense(const DenseSetup& s, void* stream) {
+  if (s.part_bytes > 0 && cudaMemsetAsync(s.p.part_count, 0, s.part_bytes, static_cast<cudaStream_t>(stream)) !=
+                              cudaSuccess)
+    return ATTN_ERR_LAUNCH;
   return launch_status(launch_dense(s.p, s.m, s.bf16, s.grid, static_cast<cudaStream_t>(stream)));
 }
 
@@ -482,6 +542,19 @@ size_t attn_bwd_workspace_size(int64_t B, int64_t S, int64_t H, int64_t Dq, int6
   return static_cast<size_t>(ws_layout(B, S, H, Dq, dkv_elems).total);
 }
 
+size_t attn_bwd_gqa_workspace_size(int64_t B, int64_t S, int64_t HQ, int64_t D) {
+  if (B < 0 || S < 0 || HQ < 0 || D < 0) return 0;
+  const int64_t tiles_bound = B * HQ * ((S + kDenseBM - 1) / kDenseBM);
+  const int64_t tiles = D == 128 ? (tiles_bound < kMaxTailTiles ? tiles_bound : kMaxTailTiles) : 0;
+  return static_cast<size_t>(ws_layout(B, S, HQ, D, tiles > 0 ? tail_region_elems(tiles, D) : 0).total);
+}
+
+void attn_bwd_tail_plan(int64_t tiles, int32_t ctas, int32_t G, int32_t* out) {
+  if (!out) return;
+  const TailPlan t = tail_plan(tiles, ctas, G);
+  out[0] = t.start, out[1] = t.tiles, out[2] = t.hpu;
+}
+
 const char* attn_bwd_status_string(attn_status_t s) {
   switch (s) {
     case ATTN_OK: return "ok";
@@ -518,7 +591,7 @@ void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_
   TileInfo ti{};
   if (B >= 1 && S >= 1 && HKV >= 1 && (!cu_seqlens || num_seqs >= 1)) {
     DenseParams p{};
-    p.B = B, p.S = S, p.Sk = S, p.HKV = HKV;
+    p.B = B, p.S = S, p.Sk = S, p.HKV = HKV, p.G = 1;
     p.tile_group = kTileGroup;
     p.causal = causal ? 1 : 0, p.window = window_left;
     p.cu_seqlens = cu_seqlens, p.num_seqs = cu_seqlens ? num_seqs : 0;
@@ -527,6 +600,23 @@ void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_
   }
   const int32_t v[7] = {ti.valid, ti.b, ti.g, ti.seq_start, ti.k0, ti.qlo, ti.nq};
   for (int i = 0; i < 7; ++i) out[i] = ti.valid ? v[i] : 0;
+}
+
+void attn_bwd_tile_schedule_split(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t G, int32_t tail_start,
+                                  int32_t tail_tiles, int32_t tail_hpu, int32_t* out) {
+  if (!out) return;
+  TileInfo ti{};
+  const bool split_ok = tail_tiles == 0 || (tail_tiles > 0 && tail_hpu >= 1 && G % tail_hpu == 0 && tail_start >= 0);
+  if (B >= 1 && S >= 1 && HKV >= 1 && G >= 1 && split_ok) {
+    DenseParams p{};
+    p.B = B, p.S = S, p.Sk = S, p.HKV = HKV, p.G = G;
+    p.tile_group = kTileGroup;
+    p.bn = kDenseBN;
+    p.tail_start = tail_start, p.tail_tiles = tail_tiles, p.tail_hpu = tail_hpu;
+    ti = decode_tile(t, p);
+  }
+  const int32_t v[10] = {ti.valid, ti.b, ti.g, ti.seq_start, ti.k0, ti.qlo, ti.nq, ti.h0, ti.hn, ti.part};
+  for (int i = 0; i < 10; ++i) out[i] = ti.valid ? v[i] : 0;
 }
 
 attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so, const void* dO, attn_strides_t sdo,
@@ -547,7 +637,9 @@ attn_status_t attn_bwd_gqa_main(const void* q, attn_strides_t sq, const void* k,
   DenseSetup s;
   const attn_status_t st = setup_dense(&s, q, sq, k, sk, v, sv, dO, sdo, B, S, HQ, HKV, D, dtype, sm_scale, mask, dk,
                                        sdk, dv, sdv, workspace, workspace_bytes);
-  return st != ATTN_OK ? st : run_dense(s, stream);
+  if (st != ATTN_OK) return st;
+  plan_tail_split(&s, workspace, workspace_bytes);
+  return run_dense(s, stream);
 }
 
 attn_status_t attn_bwd_dq_land(void* dq, attn_strides_t sdq, int64_t B, int64_t S, int64_t H, int64_t D,
@@ -569,6 +661,7 @@ attn_status_t attn_bwd_gqa(const void* q, attn_strides_t sq, const void* k, attn
   attn_status_t st = setup_dense(&main, q, sq, k, sk, v, sv, dO, sdo, B, S, HQ, HKV, D, dtype, sm_scale, mask, dk,
                                  sdk, dv, sdv, workspace, workspace_bytes);
   if (st != ATTN_OK) return st;
+  plan_tail_split(&main, workspace, workspace_bytes);
   PreSetup pre;
   st = setup_preprocess(&pre, o, so, dO, sdo, lse, slse, B, S, HQ, D, D, 0, dtype, workspace, workspace_bytes);
   if (st != ATTN_OK) return st;

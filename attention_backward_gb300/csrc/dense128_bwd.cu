@@ -230,10 +230,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
         if (!ti.valid) break;
-        const int n = p.G * ti.nq;
+        const int n = ti.hn * ti.nq;
         for (int j = 0; j < n && ok; ++j, ++gs) {
           const int st = gs % ST;
-          const int h = ti.g * p.G + j / ti.nq, c2 = ti.seq_start + (ti.qlo + j % ti.nq) * BN;
+          const int h = ti.g * p.G + ti.h0 + j / ti.nq, c2 = ti.seq_start + (ti.qlo + j % ti.nq) * BN;
           uint8_t* stg = sm + OFF_STAGE + st * STAGE;
 #pragma unroll 1
           for (int hf = 0; hf < 2; ++hf) {
@@ -332,12 +332,12 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         }
       }
       kv_pend = tc & 1;
-      const int n = p.G * ti.nq;
+      const int n = ti.hn * ti.nq;
       // LSE2 / delta of a step are loaded into registers one step ahead
       constexpr int PER_LANE = BN / 32;
       float nl[PER_LANE], nd[PER_LANE];
       auto load_rows = [&](int jj) {
-        const int hh = ti.g * p.G + jj / ti.nq, qq = (ti.qlo + jj % ti.nq) * BN;
+        const int hh = ti.g * p.G + ti.h0 + jj / ti.nq, qq = (ti.qlo + jj % ti.nq) * BN;
         const int64_t rb = (static_cast<int64_t>(ti.b) * p.HQ + hh) * p.S + ti.seq_start;
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         if (gs >= static_cast<uint32_t>(ST) &&
             !(ok = mbar_wait_warp(&bars[EMPTY0 + st], (r - 1) & 1, wc, kErrWaitStageEmpty)))
           break;
-        const int h = ti.g * p.G + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
+        const int h = ti.g * p.G + ti.h0 + j / ti.nq, q0 = (ti.qlo + j % ti.nq) * BN;
         uint8_t* sq = sm + OFF_STAGE + st * STAGE;
         int qr0, qr1;
         tail_rows(ti.seq_start + q0, BN, tail0, p.S, &qr0, &qr1);
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
         pend_full[st] = r & 1;
         // warm L2 with the operands of a step PREFETCH steps ahead
         if (j + PREFETCH < n) {
-          const int hf = ti.g * p.G + (j + PREFETCH) / ti.nq, qf = (ti.qlo + (j + PREFETCH) % ti.nq) * BN;
+          const int hf = ti.g * p.G + ti.h0 + (j + PREFETCH) / ti.nq, qf = (ti.qlo + (j + PREFETCH) % ti.nq) * BN;
           if (lane == 0) {
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
       if (!ti.valid) break;
-      const int n = p.G * ti.nq;
+      const int n = ti.hn * ti.nq;
       if (!(ok = mbar_wait_warp(&bars[KV_FULL], tc & 1, wc, kErrWaitKV))) break;
       tc_fence_after();
       for (int j = 0; j < n; ++j, ++gs) {
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
       if (!ti.valid) break;
-      const int n = p.G * ti.nq;
+      const int n = ti.hn * ti.nq;
       const int kpos = ti.k0 + row;
       const bool kvalid = kpos < ti.len;
       for (int j = 0; j < n; ++j, ++gs) {
@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[TILE_EMPTY0 + slot]);
       if (!ti.valid) break;
-      const int n = p.G * ti.nq;
+      const int n = ti.hn * ti.nq;
       for (int j = 0; j < n; ++j, ++gs) {
         const int st = gs % ST;
         // dQ complete (so dV and dK, issued before it, have read this step's stage)
@@ -783,6 +783,59 @@ __global__ void __launch_bounds__(THREADS, 1) dense128_bwd_kernel(const __grid_c
       uint8_t* const out_v = p.dv + 2 * (ti.b * p.sdv_b + pos * p.sdv_s + ti.g * p.sdv_h);
       uint8_t* const out_k = p.dk + 2 * (ti.b * p.sdk_b + pos * p.sdk_s + ti.g * p.sdk_h);
       constexpr int NCK = D / 32;  // chunks per accumulator
+      if (ti.part >= 0) {
+        // A last-round unit: add this unit's dV / dK (times sm_scale) into the
+        // tile's f32 partials, column group c4 of row q at (c4 * 128 + q) * 4, so
+        // that a warp adds 512 contiguous bytes per instruction; the warp whose
+        // add completes its row quarter over all units casts the quarter.
+        float* const acc = p.part_acc + static_cast<int64_t>(ti.part) * (2 * D * BM);
+#pragma unroll 1
+        for (int cc = 0; cc < 2 * NCK; ++cc) {
+          const float mul = cc >= NCK ? p.sm_scale : 1.f;
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + (cc >= NCK ? T_DK + (cc - NCK) * 32 : T_DV + cc * 32), r);
+          tmem_ld_wait();
+          if (cc == 2 * NCK - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[DKV_FREE]);
+          }
+          if (n > 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              red_add_f32x4(acc + (static_cast<int64_t>(cc * 8 + c4) * BM + q) * 4,
+                            __uint_as_float(r[4 * c4]) * mul, __uint_as_float(r[4 * c4 + 1]) * mul,
+                            __uint_as_float(r[4 * c4 + 2]) * mul, __uint_as_float(r[4 * c4 + 3]) * mul);
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.part_count + ti.part * 4 + quad, 1) == p.G / p.tail_hpu - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+#pragma unroll 1
+          for (int cc = 0; cc < 2 * NCK; ++cc) {
+            uint8_t* const out = cc >= NCK ? out_k : out_v;
+            const int ch = cc >= NCK ? cc - NCK : cc;
+            if (kvalid) {
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8) {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(acc) + (cc * 8 + 2 * c8) * BM + q);
+                const float4 b = __ldcg(reinterpret_cast<const float4*>(acc) + (cc * 8 + 2 * c8 + 1) * BM + q);
+                uint4 v;
+                v.x = pack2<BF16>(a.x, a.y);
+                v.y = pack2<BF16>(a.z, a.w);
+                v.z = pack2<BF16>(b.x, b.y);
+                v.w = pack2<BF16>(b.z, b.w);
+                *reinterpret_cast<uint4*>(out + 2 * (ch * 32 + c8 * 8)) = v;
+              }
+            }
+          }
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int cc = 0; cc < 2 * NCK; ++cc) {
         const bool isK = cc >= NCK;

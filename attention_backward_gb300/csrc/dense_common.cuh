@@ -11,6 +11,9 @@ namespace ab {
 struct TileInfo {
   int b, g, seq_start, len, k0, qlo, nq, valid;
   int qlen, off;
+  // query heads h0 .. h0 + hn - 1 of the group; part >= 0: a last-round unit
+  // whose dK/dV partial goes to slot ``part`` of the f32 partials
+  int h0, hn, part;
 };
 
 // TMEM column, relative to a step's S^T buffer, of the 16-bit pair of P^T
@@ -43,6 +46,9 @@ constexpr int kSplitMinGroup = 4;
 // most kTileGroup, and no more than the CTAs in flight can cover at once
 // (about one tile of every pair of the group per CTA).
 constexpr int kTileGroup = 8;
+// Most last-round tiles whose dK/dV partials a workspace holds (the last round
+// has fewer tiles than the launch has CTAs).
+constexpr int kMaxTailTiles = 256;
 __host__ __device__ inline int tile_group(int ctas, int tiles_per_pair) {
   const int g = tiles_per_pair > 0 ? ctas / tiles_per_pair : kTileGroup;
   return g < 1 ? 1 : (g > kTileGroup ? kTileGroup : g);
@@ -60,11 +66,26 @@ __host__ __device__ inline int tile_group(int ctas, int tiles_per_pair) {
 // sequences keep key block major order over all pairs (their tile count per
 // pair is known only on the device, and the draws past it end a CTA's work).
 // Host code may call it too (with cu_seqlens in host memory) to check the order.
+// Draws from p.tail_start on (when p.tail_tiles > 0) are last-round units:
+// unit u is tile p.tail_start + u % p.tail_tiles, heads from
+// (u / p.tail_tiles) * p.tail_hpu, so the units of one head slice of every
+// tail tile come before the next slice.
 static __host__ __device__ __forceinline__ TileInfo decode_tile(int t, const DenseParams& p) {
   TileInfo ti{};
   ti.valid = 0;
+  ti.h0 = 0;
+  ti.hn = p.G;
+  ti.part = -1;
   const int BH = p.B * p.HKV;
   if (t < 0) return ti;
+  if (p.tail_tiles > 0 && t >= p.tail_start) {
+    const int u = t - p.tail_start;
+    if (u >= p.tail_tiles * (p.G / p.tail_hpu)) return ti;
+    ti.part = u % p.tail_tiles;
+    ti.h0 = (u / p.tail_tiles) * p.tail_hpu;
+    ti.hn = p.tail_hpu;
+    t = p.tail_start + ti.part;
+  }
   int bh, r;
   if (p.cu_seqlens == nullptr) {
     const int nt = (p.Sk + kDenseBM - 1) / kDenseBM;  // key tiles per pair

@@ -56,6 +56,14 @@ struct DenseParams {
   int* tile_counter;  // zeroed by the preprocess; persistent CTAs draw tiles from it
   int bn;             // query rows per step (the tile schedule's query block)
   int tile_group;     // (batch, KV head) pairs drawn together, dense batches (tile_group())
+  // Last-round split (head dim 128, dense batches): the tile draws from
+  // tail_start on cover the last tail_tiles key tiles, each as G / tail_hpu
+  // units of tail_hpu query heads; a unit adds its dK/dV partial into
+  // part_acc in f32, and the last unit of each 32-row quarter of a tile
+  // casts it.  tail_tiles = 0: every tile is drawn whole.
+  int tail_start, tail_tiles, tail_hpu;
+  int* part_count;  // [tail_tiles][4] units done per row quarter (zeroed by the preprocess)
+  float* part_acc;  // [tail_tiles][2 D / 4][128 rows][4] f32, dV columns then dK (zeroed by the preprocess)
 };
 
 struct DenseMaps {

@@ -171,6 +171,11 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, const vo
       "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
       : "memory");
 }
+// Four f32 adds into global memory (16-byte aligned), performed at L2.
+__device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk group has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {

@@ -316,7 +316,7 @@ def time_dense(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
 
     tq, tk, tv, to, tdo, lse = gpu_dense_inputs(w, device)
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=device) if w.cu_seqlens else None
-    ws = ab._binding.new_workspace(w.B, w.S, w.HQ, w.D, device=device)
+    ws = ab._binding.new_gqa_workspace(w.B, w.S, w.HQ, w.D, device=device)
     dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
     stream = torch.cuda.current_stream(device)
 

@@ -118,6 +118,16 @@ typedef struct {
  * (0 for dense).  Every region is 256-byte aligned. */
 ATTN_BWD_API size_t attn_bwd_workspace_size(int64_t B, int64_t S, int64_t H, int64_t Dq, int64_t dkv_elems);
 
+/* Workspace bytes with which the one-call dense backward (attn_bwd_gqa,
+ * attn_bwd) may split the last round of key tiles: at head dim 128, on an
+ * unmasked dense batch with G >= 2, when the tiles do not divide evenly over
+ * the persistent CTAs, the last round's tiles are drawn as units of fewer query
+ * heads whose dK/dV partials are added in f32 behind the dQ accumulator (at
+ * most 256 tiles, 2*D*128 + 4 values each).  Any workspace of at least
+ * attn_bwd_workspace_size(B, S, HQ, D, 0) bytes stays valid: without room for
+ * the partials the tiles are drawn whole.  0 for negative sizes. */
+ATTN_BWD_API size_t attn_bwd_gqa_workspace_size(int64_t B, int64_t S, int64_t HQ, int64_t D);
+
 /* Split form, launch 1: delta_i = sum_d O_id dO_id (f32), LSE*log2(e), zeroed dQ (and
  * dKV) accumulators, cleared error word and tile counter.  The delta row
  * preprocess of the TileOPs page ("delta_rows" in its Base and Tiled
@@ -155,7 +165,8 @@ ATTN_BWD_API attn_status_t attn_bwd_preprocess(const void* o, attn_strides_t so,
  *   D in {64, 128};  G = HQ / HKV within the limits above;  S >= 1;  B == 1
  *   when varlen;  sm_scale finite.  Query head h reads KV head h / G.
  *   workspace : at least attn_bwd_workspace_size(B, S, HQ, D, 0) bytes,
- *   16-byte aligned, owned by the caller; its contents on entry do not matter.
+ *   16-byte aligned, owned by the caller; its contents on entry do not matter;
+ *   attn_bwd_gqa_workspace_size(B, S, HQ, D) bytes allow the last-round split.
  * Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, bad stride, size
  * or mask), ATTN_ERR_UNSUPPORTED (head dim, group size, dtype, sizes past
  * 2^31 rows), ATTN_ERR_WORKSPACE, all before anything is queued;
@@ -314,6 +325,21 @@ ATTN_BWD_API void attn_bwd_query_block_range_qk(int32_t k0, int32_t block_k, int
 ATTN_BWD_API void attn_bwd_tile_schedule(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t causal,
                                          int32_t window_left, const int32_t* cu_seqlens, int32_t num_seqs,
                                          int32_t* out);
+
+/* Host-side plan of the last-round split for ``tiles`` equal key tiles on
+ * ``ctas`` persistent CTAs with G query heads per KV head: out[0..2] =
+ * {first split draw, split tiles, query heads per unit}, all 0 when the tiles
+ * are drawn whole (the split shortens the last round by less than a quarter
+ * tile, half a tile at G = 2, or G < 2, or the tiles divide evenly). */
+ATTN_BWD_API void attn_bwd_tail_plan(int64_t tiles, int32_t ctas, int32_t G, int32_t* out);
+
+/* attn_bwd_tile_schedule for an unmasked dense batch with G query heads per KV
+ * head and a last-round split (tail_tiles = 0: none): out[0..9] = the seven
+ * values above, then {first query head of the unit within the group, query
+ * heads, partials slot (-1 for a whole tile)}. */
+ATTN_BWD_API void attn_bwd_tile_schedule_split(int32_t t, int32_t B, int32_t S, int32_t HKV, int32_t G,
+                                               int32_t tail_start, int32_t tail_tiles, int32_t tail_hpu,
+                                               int32_t* out);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on a
  * barrier nothing signals, with a ``timeout_us`` limit, and returns what

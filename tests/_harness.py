@@ -66,7 +66,7 @@ def run_dense(w, problem, poison=True, workspace=None, stream=None, split=False)
     dq = torch.full_like(tq, fill)
     dk = torch.full_like(tk, fill)
     dv = torch.full_like(tv, fill)
-    ws = workspace if workspace is not None else ab._binding.new_workspace(w.B, w.S, w.HQ, w.D)
+    ws = workspace if workspace is not None else ab._binding.new_gqa_workspace(w.B, w.S, w.HQ, w.D)
     if poison and workspace is None:
         ws.fill_(0xFF)
     if split:

@@ -136,6 +136,58 @@ def test_tile_schedule_draws_every_key_tile_once(ab, B, S, HKV, causal, window, 
             assert k0s == sorted(k0s)
 
 
+@pytest.mark.parametrize("tiles,ctas,G,want", [
+    (512, 152, 8, (456, 56, 1)),     # GQA 16384 with 4 KV heads: 3 rounds and 56 tiles, as 448 one-head units
+    (160, 152, 2, (152, 8, 1)),      # 8 tiles left over, as 16 one-head units
+    (304, 152, 8, (0, 0, 0)),        # tiles divide evenly
+    (100, 152, 8, (0, 0, 0)),        # one round
+    (160, 152, 1, (0, 0, 0)),        # one query head per KV head: nothing to split
+    (303, 152, 2, (0, 0, 0)),        # 151 tiles left over: one-head units would take as long
+    (200, 152, 4, (152, 48, 2)),     # 48 tiles as 96 two-head units: one unit round of half a tile
+])
+def test_tail_plan(ab, tiles, ctas, G, want):
+    assert ab.tail_plan(tiles, ctas, G) == want
+
+
+@pytest.mark.parametrize("B,S,HKV,G,ctas", [(1, 16384, 4, 8, 152), (1, 1000, 20, 2, 152), (2, 512, 20, 8, 152),
+                                            (3, 300, 5, 4, 7)])
+def test_split_schedule_covers_every_head_of_every_tile_once(ab, B, S, HKV, G, ctas):
+    """With the last-round split the draws cover every (batch, KV head, key
+    tile, query head) exactly once: whole tiles take all G heads, the split
+    tiles come as units of the planned head count with a partials slot per
+    tile, and the draws end together."""
+    tiles = B * HKV * ((S + 127) // 128)
+    start, ntail, hpu = ab.tail_plan(tiles, ctas, G)
+    assert ntail > 0
+    want = {(b, g, k0, h) for b in range(B) for g in range(HKV) for k0 in range(0, S, 128) for h in range(G)}
+    got, slot_tile = [], {}
+    for t in range(start + ntail * (G // hpu) + 4):
+        valid, b, g, s0, k0, qlo, nq, h0, hn, part = ab.tile_schedule_split(t, B, S, HKV, G, start, ntail, hpu)
+        if t >= start + ntail * (G // hpu):
+            assert not valid
+            continue
+        assert valid and s0 == 0 and (qlo, nq) == (0, (S + 127) // 128)
+        if t < start:
+            assert (h0, hn, part) == (0, G, -1)
+            assert ab.tile_schedule(t, B, S, HKV, False, -1)[1:5] == (b, g, 0, k0)
+        else:
+            assert hn == hpu and 0 <= part < ntail and h0 % hpu == 0
+            assert slot_tile.setdefault(part, (b, g, k0)) == (b, g, k0)
+            assert ab.tile_schedule(start + part, B, S, HKV, False, -1)[1:5] == (b, g, 0, k0)
+        got += [(b, g, k0, h) for h in range(h0, h0 + hn)]
+    assert len(got) == len(set(got)) == len(want) and set(got) == want
+    assert len(slot_tile) == ntail
+
+
+def test_gqa_workspace_holds_the_last_round_partials(ab):
+    base = ab.workspace_size(1, 16384, 32, 128)
+    # 256 tiles of 2 x 128 x 128 f32 partials and 4 counters, behind the dQ accumulator
+    assert ab.gqa_workspace_size(1, 16384, 32, 128) == base + 256 * 4 * 4 + 256 * 2 * 128 * 128 * 4
+    # at most one tile per (query head, key block) of the batch: 2 here
+    assert ab.gqa_workspace_size(1, 100, 2, 128) == ab.workspace_size(1, 100, 2, 128) + 256 + 2 * 2 * 128 * 128 * 4
+    assert ab.gqa_workspace_size(1, 4096, 8, 64) == ab.workspace_size(1, 4096, 8, 64)  # head dim 64: no split
+
+
 def test_tile_schedule_rejects_bad_sizes(ab):
     assert ab.tile_schedule(0, 0, 128, 1, True, -1)[0] == 0
     assert ab.tile_schedule(0, 1, 0, 1, True, -1)[0] == 0

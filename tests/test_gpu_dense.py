@@ -69,6 +69,39 @@ def test_small_cases_match_oracle(w):
     assert_close(dv, rv, w, "dv")
 
 
+# Unmasked dense batches whose key tiles do not divide evenly over the SMs:
+# at head dim 128 the one-call path draws the last round's tiles as units of
+# fewer query heads and adds their dK/dV in f32 (160 tiles on 152 SMs: the
+# last 8 tiles split into single-head units).  A ragged last key tile and the
+# bf16 kernel with the rounding residuals are among them.
+LAST_ROUND = [
+    inputs.scaled(C3, name="split_g2_s1024_hkv20_f16", S=1024, HQ=40, HKV=20, dtype="f16"),
+    inputs.scaled(C3, name="split_g2_s1000_hkv20_bf16", S=1000, HQ=40, HKV=20),
+    inputs.scaled(C3, name="split_g8_b2_s512_hkv20_bf16", B=2, S=512, HQ=160, HKV=20),
+]
+
+
+@pytest.mark.parametrize("w", LAST_ROUND, ids=lambda w: w.name)
+def test_last_round_split_matches_oracle(w):
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    tiles = w.B * w.HKV * ((w.S + 127) // 128)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = ab.tail_plan(tiles, min(tiles, sms), w.HQ // w.HKV)
+    if plan[1] == 0:
+        pytest.skip(f"{tiles} tiles on {sms} SMs: no last-round split")
+    prob = dense_problem(w)
+    q, k, v, o, do, lse = prob
+    rq, rk, rv = oracle.backward(q, k, v, o, do, lse, w.sm_scale, **mask_of(w))
+    for split in (False, True):  # the one-call path, then the three launches one by one
+        dq, dk, dv, _ = run_dense(w, prob, split=split)
+        assert_close(dq, rq, w, "dq")
+        assert_close(dk, rk, w, "dk")
+        assert_close(dv, rv, w, "dv")
+
+
 # Dense rows whose key length differs from the query length (kv_len in the C
 # mask): the masks are aligned at the end of the row, query i at key position
 # i + Sk - S.  Cases cover more and fewer keys than queries under every mask
