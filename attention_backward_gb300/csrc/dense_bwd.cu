@@ -596,7 +596,23 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
           return __ffma2_rn(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2,
                             make_float2(lo, hi));
         };
-        if (full_vis) {
+        // In a block that is not fully visible, my columns cc in [c_lo, c_hi) are:
+        // a real query (cc < qlen - qc0), at or after my key (kpos <= qc0 + cc +
+        // off) and within the window (qc0 + cc + off < kpos + W); one range per
+        // step, two compares a column.  A warp whose rows all see every one of
+        // their columns takes the unmasked path, one whose rows see none of them
+        // writes zeros (the diagonal and window-edge blocks hold both kinds).
+        int c_lo = 0, c_hi = HALF, mode = 0;  // mode 0: all visible, 1: none, 2: per column
+        if (!full_vis) {
+          const int64_t d0 = static_cast<int64_t>(kpos) - qc0 - ti.off;
+          const int64_t hi = W > 0 ? d0 + W : HALF;
+          c_lo = cm ? static_cast<int>(d0 < 0 ? 0 : (d0 > HALF ? HALF : d0)) : 0;
+          c_hi = imin(ti.qlen - qc0, static_cast<int>(hi < 0 ? 0 : (hi > HALF ? HALF : hi)));
+          mode = __all_sync(0xffffffffu, kvalid && c_lo == 0 && c_hi == HALF)   ? 0
+                 : __all_sync(0xffffffffu, !kvalid || c_hi <= c_lo) ? 1
+                                                                    : 2;
+        }
+        if (mode == 0) {
 #pragma unroll
           for (int c4 = 0; c4 < HALF / 4; ++c4) {
             const float4 t = lse4[c4];  // -LSE2
@@ -606,14 +622,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) dense_bwd_kernel(const __g
             pv[4 * c4 + 2] = ex2(x1.x);
             pv[4 * c4 + 3] = ex2(x1.y);
           }
+        } else if (mode == 1) {
+#pragma unroll
+          for (int cc = 0; cc < HALF; ++cc) pv[cc] = 0.f;
         } else {
-          // my columns cc in [c_lo, c_hi) are visible: a real query (cc < qlen -
-          // qc0), at or after my key (kpos <= qc0 + cc + off) and within the window
-          // (qc0 + cc + off < kpos + W); one range per step, two compares a column
-          const int64_t d0 = static_cast<int64_t>(kpos) - qc0 - ti.off;
-          const int64_t hi = W > 0 ? d0 + W : HALF;
-          const int c_lo = cm ? static_cast<int>(d0 < 0 ? 0 : (d0 > HALF ? HALF : d0)) : 0;
-          const int c_hi = imin(ti.qlen - qc0, static_cast<int>(hi < 0 ? 0 : (hi > HALF ? HALF : hi)));
 #pragma unroll
           for (int c4 = 0; c4 < HALF / 4; ++c4) {
             const float4 t = lse4[c4];  // -LSE2
