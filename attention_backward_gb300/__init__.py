@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     query_block_range,
     query_block_range_qk,
     selftest_timeout,
+    sink_grad,
     sparse_backward,
     sparse_land,
     sparse_main,

@@ -36,6 +36,7 @@ class Mask(ctypes.Structure):
 _SIGS = {
     "attn_bwd_workspace_size": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
     "attn_bwd_gqa_workspace_size": (c_sz, [c_i64, c_i64, c_i64, c_i64]),
+    "attn_bwd_sink_grad": (c_i32, [c_vp, c_i64, c_i64, c_i64, ctypes.POINTER(Mask), c_vp, c_sz, c_vp, c_vp]),
     "attn_bwd_tail_plan": (None, [c_i64, c_i32, c_i32, ctypes.POINTER(c_i32)]),
     "attn_bwd_tile_schedule_split": (None, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                                             ctypes.POINTER(c_i32)]),
@@ -155,6 +156,21 @@ def workspace_size(B: int, S: int, H: int, Dq: int, dkv_elems: int = 0) -> int:
 def new_workspace(B: int, S: int, H: int, Dq: int, dkv_elems: int = 0, device=None) -> torch.Tensor:
     n = workspace_size(B, S, H, Dq, dkv_elems)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def sink_grad(sink, workspace, B: int, S: int, cu_seqlens=None, stream=None):
+    """dsink [HQ] f32 of per-head attention-sink logits ``sink`` (f32 [HQ],
+    CUDA) from the LSE2 and delta that a dense backward call (with sink-aware
+    O and LSE) left in ``workspace`` (see attn_bwd_sink_grad)."""
+    _dev(sink, workspace)
+    if sink.dtype != torch.float32 or sink.dim() != 1 or not sink.is_contiguous():
+        raise AttnBwdError("sink must be a contiguous float32 vector")
+    HQ = sink.numel()
+    dsink = torch.empty_like(sink)
+    m = _mask(False, -1, cu_seqlens, S, S)
+    _status(library().attn_bwd_sink_grad(sink.data_ptr(), B, S, HQ, ctypes.byref(m), workspace.data_ptr(),
+                                         workspace.numel(), dsink.data_ptr(), _stream(stream)), "attn_bwd_sink_grad")
+    return dsink
 
 
 def gqa_workspace_size(B: int, S: int, HQ: int, D: int) -> int:

@@ -15,9 +15,11 @@
 #include <mutex>
 
 #include "attn_bwd.h"
+#include "attn_bwd_sink.h"
 #include "common.cuh"
 #include "dense_common.cuh"
 #include "kernels.h"
+#include "sink.h"
 
 namespace {
 
@@ -734,6 +736,28 @@ attn_status_t attn_bwd_sparse(const void* q, attn_strides_t sq, const void* kv, 
   if ((st = run_preprocess(pre, stream)) != ATTN_OK) return st;
   if ((st = run_sparse(main, stream)) != ATTN_OK) return st;
   return run_land(land, stream);
+}
+
+attn_status_t attn_bwd_sink_grad(const float* sink, int64_t B, int64_t S, int64_t HQ, const attn_mask_t* mask,
+                                 const void* workspace, size_t workspace_bytes, float* dsink, void* stream) {
+  if (!sink || !dsink || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || HQ < 1) return ATTN_ERR_INVALID_ARG;
+  if (B * S * HQ >= (int64_t(1) << 31) || HQ > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(sink) & 3u) || (reinterpret_cast<uintptr_t>(dsink) & 3u) || !aligned16(workspace))
+    return ATTN_ERR_INVALID_ARG;
+  MaskArgs ma;
+  if (const attn_status_t mst = parse_mask(mask, B, S, &ma); mst != ATTN_OK) return mst;
+  const WsLayout L = ws_layout(B, S, HQ, 0, 0);
+  if (workspace_bytes < static_cast<size_t>(L.dq_off)) return ATTN_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  SinkGradParams p{};
+  p.sink = sink;
+  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2_off);
+  p.delta = reinterpret_cast<const float*>(ws + L.delta_off);
+  p.B = static_cast<int>(B), p.S = static_cast<int>(S), p.H = static_cast<int>(HQ);
+  p.cu_seqlens = ma.cu, p.num_seqs = ma.num_seqs;
+  p.dsink = dsink;
+  return launch_status(launch_sink_grad(p, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_bwd_check_error(const void* workspace, void* stream, int32_t* device_code) {

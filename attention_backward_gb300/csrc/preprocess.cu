@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "cvt.cuh"
 #include "kernels.h"
+#include "sink.h"
 #include "sm103.cuh"
 
 namespace ab {
@@ -180,7 +181,43 @@ __global__ void __launch_bounds__(256) land_kernel(LandParams p) {
   }
 }
 
+// dsink_h = -sum over the rows of every sequence of exp(sink_h - LSE_i) delta_i:
+// one block per head, a fixed order of additions (no atomics), so that the
+// result is the same from run to run.  Rows whose LSE2 is not finite (no
+// visible key and no sink in the forward) add nothing.
+__global__ void __launch_bounds__(256) sink_grad_kernel(SinkGradParams p) {
+  const int h = blockIdx.x;
+  int r0 = 0, r1 = p.S;
+  if (p.cu_seqlens != nullptr) {
+    r0 = clamp_pos(p.cu_seqlens[0], p.S);
+    r1 = clamp_pos(p.cu_seqlens[p.num_seqs], p.S);
+  }
+  const float s2 = p.sink[h] * kLog2e;
+  float acc = 0.f;
+  for (int b = 0; b < p.B; ++b) {
+    const int64_t base = (static_cast<int64_t>(b) * p.H + h) * p.S;
+    for (int r = r0 + static_cast<int>(threadIdx.x); r < r1; r += blockDim.x) {
+      const float l2 = p.lse2[base + r];
+      if (isfinite(l2)) acc = fmaf(exp2f(s2 - l2), p.delta[base + r], acc);
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  __shared__ float part[8];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += part[w];
+    p.dsink[h] = -t;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_sink_grad(const SinkGradParams& p, cudaStream_t st) {
+  sink_grad_kernel<<<p.H, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_preprocess(const PreprocessParams& p, bool bf16, int grid, cudaStream_t st) {
   if (bf16)

@@ -4,6 +4,7 @@ from .attention import (  # noqa: F401
     delta,
     forward,
     sequences,
+    sink_grad,
     sparse_backward,
     sparse_forward,
     visible,

@@ -46,6 +46,15 @@ row per key holds both K (all DQK columns) and V (its first DV columns), and
 query t attends exactly the key rows listed in ``idx[t]``; entries outside
 [0, Skv) (the -1 padding) are not visible.  dKV_j = dK_j + [dV_j, 0].
 
+Attention sink (named among the gradients of the flash-linear-attention
+issue's "Frozen correctness contract" as dsink, without a formula; the plain
+reading): one extra logit sink_h per query head joins every row's softmax
+normalisation and carries no value, so LSE_i = log(sum_j exp(s_ij) +
+exp(sink_h)) and O_i = sum_j exp(s_ij - LSE_i) v_j.  The sink's column has
+dP = dO_i . 0 = 0, so dS_i,sink = -P_i,sink delta_i and
+dsink_h = -sum_i exp(sink_h - LSE_i) delta_i; dQ, dK and dV keep the formulas
+above with that O and LSE.
+
 The forward that produces O and LSE runs in float32 (O is rounded to the input
 dtype by the caller); the backward runs in float64.  The forward is exact
 (two passes: max, then sum), not an online softmax.
@@ -123,12 +132,14 @@ def _row_sequences(Sq: int, Sk: int, cu_seqlens):
 # --------------------------------------------------------------------------
 
 def forward(q, k, v, scale, causal=False, window=-1, cu_seqlens=None, dtype=np.float32,
-            row_chunk=2048):
+            row_chunk=2048, sink=None):
     """O [B,S,HQ,Dv] and natural-log LSE [B,HQ,S] of softmax attention over
     keys k [B,Sk,HKV,D] and values v [B,Sk,HKV,Dv] (Sk = S unless the row is
     dense; see the module notes on Sk != S).
 
-    Rows with no visible key get LSE = -inf and O = 0.
+    Rows with no visible key get LSE = -inf and O = 0.  ``sink`` (one logit per
+    query head) joins every row's normalisation (module notes): such a row then
+    gets LSE = sink_h and O = 0.
     """
     B, S, HQ, _ = q.shape
     HKV = k.shape[2]
@@ -150,9 +161,13 @@ def forward(q, k, v, scale, causal=False, window=-1, cu_seqlens=None, dtype=np.f
                 m = _visible_block(np.arange(r0, r1), cols, causal, window, off)
                 s = np.where(m, s, -np.inf)
                 mx = s.max(axis=1, keepdims=True)
+                if sink is not None:
+                    mx = np.maximum(mx, dtype(sink[h]))
                 mx = np.where(np.isfinite(mx), mx, 0)
                 e_ = np.exp(s - mx)
                 tot = e_.sum(axis=1, keepdims=True)
+                if sink is not None:
+                    tot = tot + np.exp(dtype(sink[h]) - mx)
                 with np.errstate(divide="ignore"):
                     lse[b, h, a + r0:a + r1] = (mx + np.log(tot))[:, 0]
                 p = np.where(tot > 0, e_ / np.where(tot > 0, tot, 1), 0)
@@ -253,6 +268,24 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=-1, cu_seqlens=Non
                 dk[b, res["ka"] + res["kj"], g, :] += res["dk"]
                 dv[b, res["ka"] + res["kj"], g, :] += res["dv"]
     return dq, dk, dv
+
+
+def sink_grad(o, do, lse, sink, cu_seqlens=None):
+    """dsink [HQ] in float64: -sum over the rows of every sequence (all batch
+    rows) of exp(sink_h - LSE_i) delta_i (module notes); rows whose LSE is not
+    finite add nothing."""
+    B, S, HQ, _ = o.shape
+    d = delta(o, do)
+    rows = np.zeros(S, dtype=bool)
+    for a, e in sequences(S, cu_seqlens):
+        rows[a:e] = True
+    out = np.zeros(HQ)
+    for h in range(HQ):
+        l = lse[:, h, :].astype(np.float64)[:, rows]
+        ok = np.isfinite(l)
+        w = np.where(ok, np.exp(float(sink[h]) - np.where(ok, l, 0.0)), 0.0)
+        out[h] = -(w * d[:, h, rows]).sum()
+    return out
 
 
 def delta(o, do):

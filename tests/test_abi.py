@@ -23,7 +23,9 @@ def ab():
 
 
 def declared_symbols():
-    src = open(os.path.join(ROOT, "include", "attn_bwd.h")).read()
+    """Every entry point the public headers (include/*.h) declare."""
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     return sorted(set(re.findall(r"ATTN_BWD_API\s+[\w\s\*]+?\b(attn_(?:bwd|fwd)\w*)\s*\(", src)))
 
 
@@ -192,6 +194,22 @@ def test_tile_schedule_rejects_bad_sizes(ab):
     assert ab.tile_schedule(0, 0, 128, 1, True, -1)[0] == 0
     assert ab.tile_schedule(0, 1, 0, 1, True, -1)[0] == 0
     assert ab.tile_schedule(-1, 1, 128, 1, True, -1)[0] == 0
+
+
+def test_sink_grad_rejects_bad_calls_before_any_launch(ab):
+    lib = ab.library()
+    fake = 1 << 20
+    m = ab._binding.Mask(0, -1, None, 0)
+    ws = ab.workspace_size(2, 100, 4, 0)
+
+    def call(sink=fake, B=2, S=100, H=4, mask=m, ws_ptr=fake, ws_bytes=ws, dsink=fake):
+        return lib.attn_bwd_sink_grad(sink, B, S, H, ctypes.byref(mask), ws_ptr, ws_bytes, dsink, None)
+
+    assert call(sink=None) == 1 and call(dsink=None) == 1 and call(ws_ptr=None) == 1   # null pointers
+    assert call(sink=fake + 2) == 1 and call(ws_ptr=fake + 4) == 1                      # misaligned
+    assert call(B=0) == 1 and call(H=0) == 1
+    assert call(ws_bytes=ws - 512) == 3                                                # no room for LSE2 / delta
+    assert call(mask=ab._binding.Mask(0, -1, fake, 2)) == 1                            # packed rows with B > 1
 
 
 def test_argument_errors_return_before_any_launch(ab):

@@ -338,3 +338,55 @@ def test_delta_is_rowwise_dot():
     d = oracle.delta(o, do)
     assert d.shape == (1, 2, 2)
     assert d[0, 0, 0] == 0 + 1 + 2 and d[0, 1, 1] == 9 + 10 + 11 and d[0, 1, 0] == 3 + 4 + 5
+
+
+# attention sinks: one logit per query head in every row's normalisation, no value
+SINK_CASES = [
+    dict(B=1, S=5, HQ=2, HKV=1, mask=dict(causal=False)),
+    dict(B=2, S=4, HQ=2, HKV=2, mask=dict(causal=True)),
+    dict(B=1, S=7, HQ=4, HKV=2, mask=dict(causal=True, window=2, cu_seqlens=(0, 3, 7))),
+]
+
+
+@pytest.mark.parametrize("case", SINK_CASES, ids=lambda c: f"S{c['S']}H{c['HQ']}/{c['HKV']}{c['mask']}")
+def test_sink_gradients_match_finite_differences(case):
+    """With sinks in the forward, dsink and dQ, dK, dV (the backward given the
+    sink-aware O and LSE) equal the central differences of L = sum(O * dO)."""
+    rng = np.random.default_rng(11)
+    B, S, HQ, HKV = (case[x] for x in ("B", "S", "HQ", "HKV"))
+    D = 3
+    q, k = _rand(rng, B, S, HQ, D), _rand(rng, B, S, HKV, D)
+    v, do = _rand(rng, B, S, HKV, D), _rand(rng, B, S, HQ, D)
+    sink = rng.standard_normal(HQ)
+    scale = 0.8
+    mask = case["mask"]
+    o, lse = oracle.forward(q, k, v, scale, dtype=np.float64, sink=sink, **mask)
+
+    def loss():
+        o_, _ = oracle.forward(q, k, v, scale, dtype=np.float64, sink=sink, **mask)
+        return float((o_ * do).sum())
+
+    np.testing.assert_allclose(oracle.sink_grad(o, do, lse, sink, mask.get("cu_seqlens")), _fd_grad(loss, sink),
+                               rtol=1e-6, atol=1e-9)
+    dq, dk, dv = oracle.backward(q, k, v, o, do, lse, scale, **mask)
+    for got, x in ((dq, q), (dk, k), (dv, v)):
+        np.testing.assert_allclose(got, _fd_grad(loss, x), rtol=1e-6, atol=1e-8)
+
+
+def test_sink_limits():
+    """A sink at -inf is no sink; a row that sees no key puts all its mass on
+    the sink (LSE = sink, O = 0); one key and a sink give the two-way softmax."""
+    rng = np.random.default_rng(3)
+    q, k, v = _rand(rng, 1, 4, 2, 3), _rand(rng, 1, 4, 1, 3), _rand(rng, 1, 4, 1, 3)
+    o0, l0 = oracle.forward(q, k, v, 0.5, dtype=np.float64, causal=True)
+    o1, l1 = oracle.forward(q, k, v, 0.5, dtype=np.float64, causal=True, sink=np.array([-np.inf, -np.inf]))
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+    # fewer keys than queries, end-aligned causal: query 0 sees no key
+    o2, l2 = oracle.forward(q, k[:, :2], v[:, :2], 0.5, dtype=np.float64, causal=True, sink=np.array([0.25, -1.0]))
+    assert l2[0, 0, 0] == 0.25 and l2[0, 1, 0] == -1.0 and not o2[0, 0].any()
+    # query 2 sees key 0 only: O = v0 * e^s / (e^s + e^sink)
+    s = 0.5 * float(q[0, 2, 0] @ k[0, 0, 0])
+    p = math.exp(s) / (math.exp(s) + math.exp(0.25))
+    np.testing.assert_allclose(o2[0, 2, 0], p * v[0, 0, 0], rtol=1e-12)
+    np.testing.assert_allclose(l2[0, 0, 2], math.log(math.exp(s) + math.exp(0.25)), rtol=1e-12)
