@@ -183,9 +183,12 @@ __global__ void __launch_bounds__(256) land_kernel(LandParams p) {
 
 // dsink_h = -sum over the rows of every sequence of exp(sink_h - LSE_i) delta_i:
 // one block per head, a fixed order of additions (no atomics), so that the
-// result is the same from run to run.  Rows whose LSE2 is not finite (no
-// visible key and no sink in the forward) add nothing.
-__global__ void __launch_bounds__(256) sink_grad_kernel(SinkGradParams p) {
+// result is the same from run to run.  The data is small (8 bytes a row), so
+// the block is wide and each thread keeps kSinkRows independent row loads in
+// flight.  Rows whose LSE2 is not finite (no visible key and no sink in the
+// forward) add nothing.
+constexpr int kSinkThreads = 1024, kSinkRows = 4;
+__global__ void __launch_bounds__(kSinkThreads) sink_grad_kernel(SinkGradParams p) {
   const int h = blockIdx.x;
   int r0 = 0, r1 = p.S;
   if (p.cu_seqlens != nullptr) {
@@ -196,18 +199,26 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(SinkGradParams p) {
   float acc = 0.f;
   for (int b = 0; b < p.B; ++b) {
     const int64_t base = (static_cast<int64_t>(b) * p.H + h) * p.S;
-    for (int r = r0 + static_cast<int>(threadIdx.x); r < r1; r += blockDim.x) {
-      const float l2 = p.lse2[base + r];
-      if (isfinite(l2)) acc = fmaf(exp2f(s2 - l2), p.delta[base + r], acc);
+    for (int r = r0 + static_cast<int>(threadIdx.x); r < r1; r += kSinkThreads * kSinkRows) {
+      float l2[kSinkRows], dl[kSinkRows];
+#pragma unroll
+      for (int k = 0; k < kSinkRows; ++k) {
+        const int rr = r + k * kSinkThreads;
+        l2[k] = rr < r1 ? p.lse2[base + rr] : -INFINITY;
+        dl[k] = rr < r1 ? p.delta[base + rr] : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < kSinkRows; ++k)
+        if (isfinite(l2[k])) acc = fmaf(exp2f(s2 - l2[k]), dl[k], acc);
     }
   }
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  __shared__ float part[8];
+  __shared__ float part[kSinkThreads / 32];
   if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += part[w];
+    for (int w = 0; w < kSinkThreads / 32; ++w) t += part[w];
     p.dsink[h] = -t;
   }
 }
@@ -215,7 +226,7 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(SinkGradParams p) {
 }  // namespace
 
 cudaError_t launch_sink_grad(const SinkGradParams& p, cudaStream_t st) {
-  sink_grad_kernel<<<p.H, 256, 0, st>>>(p);
+  sink_grad_kernel<<<p.H, kSinkThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 

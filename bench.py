@@ -230,6 +230,27 @@ def time_forward(w, tensors, steps, warmup, device, flush_bytes=256 << 20):
     return {"ms": float(np.mean(ts)), "ms_pct": _pct(ts)}
 
 
+def time_sink_grad(w, ws, cu, steps, warmup, device, flush_bytes=256 << 20):
+    """The attention-sink gradient (attn_bwd_sink_grad) timed alone on the rows
+    a backward call left in ``ws``: events around each call, L2 flushed before
+    each.  Seeded sink logits, one per query head."""
+    import torch
+
+    import attention_backward_gb300 as ab
+
+    sink = torch.from_numpy(np.random.default_rng(w.seed).standard_normal(w.HQ).astype(np.float32)).to(device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev):
+        ev[0].record(stream)
+        ab.sink_grad(sink, ws, w.B, w.S, cu, stream)
+        ev[1].record(stream)
+
+    per = _timed_steps(step, steps, warmup, device, stream, ws, 2, flush_bytes, 1)
+    ts = [e[0].elapsed_time(e[1]) for e in per]
+    return {"ms": float(np.mean(ts)), "ms_pct": _pct(ts)}
+
+
 def gpu_sparse_inputs(w, device):
     """Q, KV, dO and the index lists from the seeded generator; O and LSE from a
     float32 torch forward over the listed rows on the device (not timed)."""
@@ -337,8 +358,9 @@ def time_dense(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
     per = _timed_steps(step, steps, warmup, device, stream, ws, 2, flush_bytes, world)
     per_st = _timed_steps(staged, steps, warmup, device, stream, ws, 4, flush_bytes, world)
     tensors = (tq, tk, tv, to, tdo, lse, cu)
+    sink = time_sink_grad(w, ws, cu, steps, warmup, device, flush_bytes)
     fwd = time_forward(w, tensors, steps, warmup, device, flush_bytes)
-    return _stage_times(per, per_st) | {"tensors": tensors, "forward": fwd}
+    return _stage_times(per, per_st) | {"tensors": tensors, "forward": fwd, "sink_grad": sink}
 
 
 def time_sparse(w, steps, warmup, device, world=1, flush_bytes=256 << 20):
@@ -645,6 +667,17 @@ def describe(w, r, pk, pk_kind, world=1):
                              "frac": fach / peak, "kernel": fname, "kernel_ms": fms,
                              "peak_kind": f"bf16 burst, {pk_kind}",
                              "traffic": traffic_record(_os.path.join(csrc, "dense_fwd.cu"), fname + "@" + w.name)}}
+        if "sink_grad" in r:  # dsink from the workspace rows: reads LSE2 and delta of every row once
+            rows = w.B * w.HQ * (w.S if w.cu_seqlens is None else w.cu_seqlens[-1] - w.cu_seqlens[0])
+            sbytes = rows * 8 + w.HQ * 8
+            sms = r["sink_grad"]["ms"]
+            hbm = float(pk["hbm_gbs"])
+            out["sink_grad"] = {
+                "ms": sms, "ms_pct": r["sink_grad"]["ms_pct"], "bytes": sbytes,
+                "roofline": {"bound": "hbm", "achieved": sbytes / (sms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                             "frac": sbytes / (sms * 1e-3) / 1e9 / hbm, "kernel": "sink_grad_kernel",
+                             "kernel_ms": sms, "peak_kind": f"copy, {pk_kind}", "traffic": None,
+                             "note": "one block per query head over a few MB: launch- and latency-bound"}}
     roof["traffic"] = traffic_record(src, kname + "@" + w.name)
     roof["peak_kind"] = f"{'bf16 burst' if roof['bound'] == 'tensor' else 'copy'}, {pk_kind}"
     roof["kernel"] = kname
@@ -719,6 +752,7 @@ def main():
         line["TFLOP/s"] = d["TFLOP/s"]
     else:
         line["forward"] = d.get("forward")
+        line["sink_grad"] = d.get("sink_grad")
     if not args.no_e2e:
         e2e_ms, h2d, d2h = time_e2e(w, r["tensors"], max(3, args.steps // 4), device)
         per_step = d["value"] * r["ms_step"] / world  # this rank's units per step
