@@ -151,6 +151,26 @@ def test_tail_plan(ab, tiles, ctas, G, want):
     assert ab.tail_plan(tiles, ctas, G) == want
 
 
+def test_tail_plan_is_the_best_split_by_brute_force(ab):
+    """Over a grid of tile counts, CTA counts and group sizes: a plan is taken
+    only when its makespan (in 1/G tiles) beats drawing whole tiles by the
+    stated margin, and no other head count per unit does better."""
+    for G in (1, 2, 3, 4, 6, 8, 12, 16):
+        for ctas in (1, 5, 7, 148, 152):
+            for T in list(range(1, 40)) + [151, 152, 153, 160, 200, 303, 304, 456, 512, 1000]:
+                start, ntail, hpu = ab.tail_plan(T, ctas, G)
+                full, R = divmod(T, ctas)
+                whole = (full + (1 if R else 0)) * G
+                options = {h: full * G + -(-(R * (G // h)) // ctas) * h for h in range(1, G) if G % h == 0}
+                best = min(options.values()) if options and R and T > ctas else whole
+                if ntail == 0:
+                    assert G < 2 or T <= ctas or R == 0 or R > 256 or whole - best < max(1, G // 4), (T, ctas, G)
+                else:
+                    assert (start, ntail) == (T - R, R) and G % hpu == 0 and hpu < G
+                    assert options[hpu] == best and whole - best >= max(1, G // 4)
+                    assert hpu == max(h for h, v in options.items() if v == best)
+
+
 @pytest.mark.parametrize("B,S,HKV,G,ctas", [(1, 16384, 4, 8, 152), (1, 1000, 20, 2, 152), (2, 512, 20, 8, 152),
                                             (3, 300, 5, 4, 7)])
 def test_split_schedule_covers_every_head_of_every_tile_once(ab, B, S, HKV, G, ctas):
